@@ -1,0 +1,224 @@
+/*
+ * gemmpipe.h -- C ABI of libgemmpipe: the software-pipelined tiled GEMM
+ * C = A * B on one NVIDIA GB300 (compute capability 10.3, sm_103a).
+ *
+ * The operation.  "Pipeline GPU Kernel" (skill page), opening summary and
+ * Step 3: a tiled GEMM whose K loop is restructured so that the global loads
+ * of K-tile n+1 overlap the tensor-core math on K-tile n.  The page works on
+ * INT8 IGEMM (int32 accumulate) and FP16 HMMA GEMMs with A of shape M x K,
+ * B of shape K x N and BM/BN/BK tiling.  Step 5 states that the pipelining
+ * leaves the arithmetic unchanged, so each entry point's result is the plain
+ * matrix product:
+ *
+ *     C[i][j] = sum over k < K of A[i][k] * B[k][j]
+ *
+ * Layout (every matrix): row-major and densely packed.
+ *     A: M x K, element (i, k) at A[i*K + k]
+ *     B: K x N, element (k, j) at B[k*N + j]
+ *     C: M x N, element (i, j) at C[i*N + j]
+ * C is overwritten (no alpha/beta: the pages define none).  A, B and C must
+ * not overlap.  No alignment beyond the element size is required; inputs
+ * whose base or row pitch is not a multiple of 16 bytes take a slower
+ * producer path (bounds-checked loads instead of the tensor-memory
+ * accelerator), with identical results.
+ *
+ * Ownership: the caller allocates A, B and C in device memory (cudaMalloc,
+ * or managed memory) on the current device and keeps them alive until the
+ * work on `stream` has finished.  gemm_f16f32 allocates nothing.
+ * gemm_s8s8s32 keeps a library-owned device workspace (the operands widened
+ * to fp16, see its comment), allocated on first use with cudaMalloc, grown
+ * when a larger problem needs it, one per (device, stream), released by
+ * gemmpipe_release_workspaces() or at unload.
+ *
+ * Execution: every GEMM call is asynchronous on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream) and targets the current CUDA device.
+ * A return of GEMMPIPE_OK means "validated and enqueued".  Errors found on
+ * the device (a pipeline wait that ran out of time) are reported later by
+ * gemmpipe_get_device_status().  No C++ exception crosses this interface.
+ * Calls may come from several host threads; the library's own state is
+ * guarded by a mutex.
+ *
+ * Error behaviour common to the GEMM entry points:
+ *   - M, N or K negative, any of them above 2^31 - 1, a null A/B with
+ *     M*N*K > 0, a null C with M*N > 0, a pointer not aligned to its element
+ *     size, or a pointer the CUDA runtime does not know as device or managed
+ *     memory                                   -> GEMMPIPE_ERR_INVALID_VALUE
+ *   - M == 0 or N == 0                         -> GEMMPIPE_OK, nothing launched
+ *   - K == 0 (the empty sum)                   -> C is set to zero
+ *   - current device is not compute capability 10.3, or no CUDA device
+ *                                              -> GEMMPIPE_ERR_UNSUPPORTED_DEVICE
+ *   - a kernel launch is refused               -> GEMMPIPE_ERR_LAUNCH
+ *   - workspace allocation fails               -> GEMMPIPE_ERR_OUT_OF_MEMORY
+ */
+#ifndef GEMMPIPE_H
+#define GEMMPIPE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMMPIPE_API __attribute__((visibility("default")))
+#else
+#define GEMMPIPE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *gemmpipe_stream_t;
+
+/* IEEE 754 binary16 value stored as its 16-bit pattern (same bits as __half). */
+typedef uint16_t gemmpipe_half_t;
+
+typedef enum {
+    GEMMPIPE_OK = 0,
+    GEMMPIPE_ERR_INVALID_VALUE = 1,
+    GEMMPIPE_ERR_UNSUPPORTED_DEVICE = 2,
+    GEMMPIPE_ERR_LAUNCH = 3,
+    GEMMPIPE_ERR_TIMEOUT = 4,
+    GEMMPIPE_ERR_INTERNAL = 5,
+    GEMMPIPE_ERR_OUT_OF_MEMORY = 6
+} gemmpipe_status_t;
+
+/*
+ * INT8 x INT8 -> INT32 GEMM, the pages' IGEMM ("Pipeline GPU Kernel", Step 2,
+ * decision thresholds measured on an INT8 IGEMM at 4096^3; "Analyze Kernel
+ * Bottleneck", Step 4, the IGEMM reference point).
+ *
+ * A: M x K int8, B: K x N int8, C: M x N int32; exact integer result.
+ * Entries whose exact value does not fit int32 wrap modulo 2^32 (for int8
+ * operands that needs K > 131071).
+ *
+ * sm_103a has no integer tcgen05 MMA, so the operands are widened to fp16
+ * (every int8 value is exact in fp16) into the library workspace, 2*(M*Kp +
+ * K*Np) bytes with Kp, Np = K, N rounded up to a multiple of 8, and
+ * multiplied on the fp16 tensor-core path with fp32 accumulation in chunks of
+ * at most 1024 k values.  Each chunk's partial sums are integers of magnitude
+ * <= 2^24, exact in fp32; the epilogue converts them to int32 and adds them.
+ * Calls on one stream share that stream's workspace and are ordered by it.
+ */
+GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K,
+                               const int8_t *A, const int8_t *B, int32_t *C,
+                               gemmpipe_stream_t stream);
+
+/*
+ * FP16 x FP16 -> FP32 GEMM, the pages' HMMA GEMM ("Analyze Kernel
+ * Bottleneck", Step 2 peak table, FP16 tensor core; "Pipeline GPU Kernel",
+ * Step 5 tolerances for FP16 tensor-core results).
+ *
+ * A: M x K binary16, B: K x N binary16, C: M x N binary32.  Products are
+ * accumulated in fp32 on the tensor cores; the summation order differs from
+ * a sequential sum, so results agree with an fp64 reference to within fp32
+ * accumulation error.  Allocates nothing.
+ */
+GEMMPIPE_API gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K,
+                              const gemmpipe_half_t *A, const gemmpipe_half_t *B,
+                              float *C, gemmpipe_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error
+ * word.  Returns GEMMPIPE_ERR_TIMEOUT if a kernel of this library gave up on
+ * a pipeline wait (every wait is bounded; the kernel then stops issuing
+ * work, drains what it issued, frees its tensor memory and exits, leaving
+ * the CUDA context usable; that call's C is undefined), GEMMPIPE_ERR_LAUNCH
+ * if the CUDA runtime reports an error for the stream, else GEMMPIPE_OK.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_get_device_status(gemmpipe_stream_t stream);
+
+/* Static, never-null English name of a status code. */
+GEMMPIPE_API const char *gemmpipe_status_string(gemmpipe_status_t status);
+
+/*
+ * "Pipeline GPU Kernel", Step 2: the per-tile compute/load ratio
+ *     2*BM*BN*BK / ((BM*BK + BK*BN) * elem_bytes)
+ * (two flops per multiply-add over the bytes of one A tile and one B tile).
+ * Returns a negative value if any argument is < 1.
+ */
+GEMMPIPE_API double gemmpipe_compute_load_ratio(int BM, int BN, int BK, int elem_bytes);
+
+/*
+ * "Pipeline GPU Kernel", Step 1, generalised from the page's double buffer to
+ * an S-stage ring: stages * (BM*BK + BK*BN) * elem_bytes, the operand bytes
+ * of the shared-memory ring (stages = 2 is the page's smem_doubled).
+ * Returns -1 if any argument is < 1.
+ */
+GEMMPIPE_API int64_t gemmpipe_stage_smem_bytes(int BM, int BN, int BK, int elem_bytes, int stages);
+
+/* Kernel plan chosen for one call; filled by gemmpipe_plan(). */
+typedef struct {
+    int producer;        /* 0: TMA producer warp, 1: bounded-load (LDG) producer warps */
+    int BM, BN, BK;      /* output tile and k-block */
+    int stages;          /* depth S of the shared-memory ring */
+    int k_chunk;         /* k values accumulated in one TMEM accumulator before a drain */
+    int threads;         /* threads per CTA */
+    int grid;            /* persistent CTAs launched */
+    int64_t tiles;       /* output tiles */
+    int64_t k_blocks;    /* ceil(K / BK) */
+    int64_t smem_bytes;  /* dynamic shared memory per CTA */
+    int vector_store;    /* 1: 16-byte stores of C, 0: 4-byte stores */
+    int64_t workspace_bytes; /* library workspace the call needs (INT8 only) */
+} gemmpipe_plan_t;
+
+/*
+ * Fills *plan with the kernel configuration that gemm_s8s8s32 (dtype 0) or
+ * gemm_f16f32 (dtype 1) would use for these arguments on the current device.
+ * Launches nothing.  Same argument checks as the GEMM calls.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K,
+                                const void *A, const void *B, const void *C,
+                                gemmpipe_plan_t *plan);
+
+/*
+ * Overrides the plan for the following calls of this process (tests and the
+ * stage/producer ablation).  producer: -1 automatic, 0 TMA (only honoured
+ * where TMA can describe the operands), 1 bounded-load producer.  bn: 0
+ * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
+ * depths (see gemmpipe_plan for what was taken).  Returns INVALID_VALUE for
+ * values outside these sets.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages);
+
+/* Frees every INT8 workspace (synchronizes the device first). */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_release_workspaces(void);
+
+/*
+ * Kernel timing.  While enabled, every GEMM call records a CUDA event pair on
+ * its stream around its main tensor-core kernel, and another around its
+ * auxiliary kernels (INT8 widening, zero fill).  gemmpipe_timing_read waits
+ * for the recorded events, returns the summed milliseconds and counts since
+ * the previous read (any pointer may be NULL) and clears them.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_timing_enable(int enable);
+GEMMPIPE_API gemmpipe_status_t gemmpipe_timing_read(double *gemm_ms, int64_t *gemm_launches,
+                                       double *aux_ms, int64_t *aux_launches);
+
+/* Total number of kernels this library has launched in this process. */
+GEMMPIPE_API int64_t gemmpipe_launch_count(void);
+
+/*
+ * Device-to-device copy of `bytes` bytes by a plain streaming kernel (16-byte
+ * accesses when both pointers and the size allow, else 1-byte).  It is the
+ * in-run HBM bandwidth reference (blog page "Fixing a GPU kernel by hand --
+ * making a transpose kernel 5x faster", section "Practice": a plain copy is
+ * measured first as the upper bound of a memory-bound kernel).
+ * Asynchronous on `stream`.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_copy(void *dst, const void *src, int64_t bytes,
+                                gemmpipe_stream_t stream);
+
+/*
+ * Test hook for the bounded waits.  For the next GEMM launch only, CTA 0's
+ * producer leaves its k-block number `k_block` (counted over the CTA's whole
+ * schedule) unfilled, and every pipeline wait of that launch gives up after
+ * `timeout_ms` milliseconds.  The consumer's wait therefore runs out; the
+ * kernel records GEMMPIPE_ERR_TIMEOUT and exits cleanly.  k_block < 0 clears
+ * the hook.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMMPIPE_H */

@@ -1,0 +1,19 @@
+// gemm_f16.cu -- fp16 x fp16 -> fp32 variants of the pipelined GEMM.
+#include "launch_impl.cuh"
+
+namespace gp {
+
+static const Variant kF16Variants[] = {
+    make_variant<GemmCfg<256, 4, false, false>>(),  // TMA producer, 128x256 tiles
+    make_variant<GemmCfg<128, 6, false, false>>(),  // TMA producer, 128x128 tiles (N <= 128)
+    make_variant<GemmCfg<256, 4, true, false>>(),   // bounded-load producer (misaligned inputs)
+    make_variant<GemmCfg<128, 6, true, false>>(),
+};
+
+int variants_f16(const Variant **out)
+{
+    *out = kF16Variants;
+    return static_cast<int>(sizeof(kF16Variants) / sizeof(kF16Variants[0]));
+}
+
+}  // namespace gp

@@ -1,0 +1,538 @@
+// gemm_kernel.cuh -- the software-pipelined tiled GEMM C = A * B for sm_103a.
+//
+// "Pipeline GPU Kernel" (skill page), Steps 3-4, turns a sequential
+// load / sync / compute / sync K loop into a prologue, a main loop that loads
+// K-tile n+1 while the tensor cores work on K-tile n, and an epilogue that
+// computes the last tile, with two shared-memory buffers used alternately.
+// Here the same schedule is spread over warps with separate jobs and the
+// double buffer becomes an S-stage ring guarded by mbarriers:
+//
+//   producer  (1 warp issuing TMA tile loads, or 8 warps doing bounds-checked
+//             loads into registers and shared-memory stores -- the page's
+//             LDG-register variant, used when TMA cannot describe the input)
+//             waits empty[s], fills stage s with the A tile (BM x BK) and the
+//             B tile (BK x BN) of k-block kb, and signals full[s];
+//   issuer    (one thread) waits full[s], issues BK/16 tcgen05.mma
+//             (M = 128, N = BN, K = 16) into a TMEM accumulator, then
+//             tcgen05.commit -> empty[s] returns the stage to the producer
+//             as soon as the tensor cores have read it;
+//   epilogue  (8 warps) waits tfull[b], reads the accumulator with
+//             tcgen05.ld, and stores C through a per-warp staging tile so
+//             that the global stores are row-contiguous.
+//
+// The page's prologue is the producer running up to S stages ahead; its
+// "compute the last tile" epilogue is the issuer's final commit on tfull.
+// Two TMEM accumulators let tile t+1's MMAs run while tile t is stored.
+//
+// For the INT8 path (operands widened to fp16, see the C header) an
+// accumulator covers at most `kb_per_chunk` k-blocks; the epilogue turns
+// each chunk's exact fp32 integers into int32 and sums them in registers.
+//
+// Every wait is bounded (globaltimer); a role that gives up records a
+// timeout in the device status word, raises the CTA's abort flag, drains
+// what it issued and returns, so the CTA always reaches its teardown and
+// frees its tensor memory.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace gp {
+
+constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
+
+template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_>
+struct GemmCfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int BK = 64;  // 64 fp16 = 128 bytes = one swizzle-atom row
+    static constexpr int STAGES = STAGES_;
+    static constexpr bool LDG = LDG_;
+    static constexpr bool INT_OUT = INT_OUT_;
+
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int NB64 = BN / 64;  // 64-column B atoms per stage
+
+    static constexpr int PRODUCER_WARPS = LDG ? 8 : 1;
+    static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
+    static constexpr int MMA_WARP = PRODUCER_WARPS;
+    static constexpr int EPI_WARP0 = MMA_WARP + 1;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI_WARPS);
+    static constexpr int EPI_COLS = BN / 2;  // columns per epilogue warp
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+
+    static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
+    static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
+    static constexpr int CTL_OFF = STAGING_OFF + STAGING_BYTES;
+    static constexpr int CTL_BYTES = 8 * (2 * STAGES + 5) + 16;
+    static constexpr int SMEM_BYTES = 1024 + CTL_OFF + CTL_BYTES;  // + alignment slack
+
+    static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
+    static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
+    static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
+};
+
+template <int STAGES>
+struct Ctl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Bounded mbarrier wait.  False when the CTA is aborting or the wait ran out
+// of time (then it records the timeout and raises the abort flag).
+struct Waiter {
+    volatile int *abort;
+    int *status;
+    uint64_t timeout_ns;
+
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const
+    {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((i & 15u) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    *abort = 1;
+                    atomicCAS(status, 0, kStatusTimeout);
+                    return false;
+                }
+            }
+        }
+    }
+
+    // Used only while draining after an abort: ignores the abort flag.
+    __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
+    {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity))
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        return true;
+    }
+};
+
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
+
+// ------------------------------------------------------------ TMA producer
+
+template <class Cfg>
+__device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
+                             uint32_t sbase, Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+{
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arm
+    int64_t kb_count = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+        const int32_t m0 = static_cast<int32_t>((t % p.m_tiles) * Cfg::BM);
+        const int32_t n0 = static_cast<int32_t>((t / p.m_tiles) * Cfg::BN);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+            if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) {
+                const uint32_t fb = smem_u32(&ctl->full[stage]);
+                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
+                const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
+                mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                tma_load_2d(sa, tA, fb, k0, m0);
+#pragma unroll
+                for (int j = 0; j < Cfg::NB64; ++j)
+                    tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                armed |= 1u << stage;
+                armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
+            }
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Let every copy this thread started land before the CTA exits.
+        for (int s = 0; s < Cfg::STAGES; ++s)
+            if (armed & (1u << s))
+                w.wait_drain(smem_u32(&ctl->full[s]), (armed_par >> s) & 1u, kDrainNs);
+    }
+}
+
+// ------------------------------------------------- bounded-load producer
+//
+// The page's LDG-register variant, moved onto producer warps: each k-block's
+// A and B tiles are read from global memory into registers with plain loads,
+// then stored into the stage in the same swizzled layout TMA would write.
+// Works for any 2-byte alignment of base and pitch: a row segment of 64 fp16
+// (128 bytes) is fetched by 8 lanes as naturally aligned 16-byte words, each
+// containing at least one byte of the row (so never outside the allocation),
+// realigned across neighbouring lanes with shuffles and funnel shifts, and
+// masked to zero outside the matrix (rows >= M or K, columns >= K or N).
+
+__device__ __forceinline__ void realign16(const uint4 &lo, const uint4 &hi, uint32_t s, uint32_t (&o)[4])
+{
+    // o = bytes [s, s + 16) of the 32-byte window lo:hi (s even, 0..14)
+    const uint32_t q = s >> 2, sh = (s & 3u) * 8u;
+    uint32_t a0, a1, a2, a3, a4;
+    if (q == 0) {
+        a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x;
+    } else if (q == 1) {
+        a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y;
+    } else if (q == 2) {
+        a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z;
+    } else {
+        a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w;
+    }
+    o[0] = __funnelshift_r(a0, a1, sh);
+    o[1] = __funnelshift_r(a1, a2, sh);
+    o[2] = __funnelshift_r(a2, a3, sh);
+    o[3] = __funnelshift_r(a3, a4, sh);
+}
+
+struct SegLoad {
+    uint4 lo, ex;
+    uint32_t s;
+    int nvalid;  // valid fp16 of this lane's 8 (0..8)
+};
+
+// Lane j of an 8-lane group, row segment starting at element e0 of a row of
+// L valid elements (row_ok false: whole segment is zero).
+__device__ __forceinline__ SegLoad seg_issue(const uint16_t *rowp, bool row_ok, int64_t e0, int64_t L, int j)
+{
+    SegLoad r;
+    r.lo = make_uint4(0, 0, 0, 0);
+    r.ex = make_uint4(0, 0, 0, 0);
+    r.s = 0;
+    r.nvalid = 0;
+    if (row_ok) {
+        const uintptr_t vlo = reinterpret_cast<uintptr_t>(rowp);
+        const uintptr_t vhi = vlo + 2 * static_cast<uintptr_t>(L);
+        const uintptr_t seg = vlo + 2 * static_cast<uintptr_t>(e0);
+        r.s = static_cast<uint32_t>(seg & 15u);
+        const uintptr_t base = seg - r.s;
+        const uintptr_t a0 = base + 16 * static_cast<uintptr_t>(j);
+        if (a0 < vhi && a0 + 16 > vlo) r.lo = ldg_nc_v4(reinterpret_cast<const void *>(a0));
+        if (j == 7 && r.s != 0) {
+            const uintptr_t a1 = base + 128;
+            if (a1 < vhi && a1 + 16 > vlo) r.ex = ldg_nc_v4(reinterpret_cast<const void *>(a1));
+        }
+        const int64_t left = L - (e0 + 8 * j);
+        r.nvalid = left <= 0 ? 0 : (left >= 8 ? 8 : static_cast<int>(left));
+    }
+    return r;
+}
+
+// All 32 lanes must call this (shuffles).  Stores the lane's 16 bytes.
+__device__ __forceinline__ void seg_store(const SegLoad &r, int j, uint32_t dst)
+{
+    uint4 hi;
+    hi.x = __shfl_down_sync(0xffffffffu, r.lo.x, 1, 8);
+    hi.y = __shfl_down_sync(0xffffffffu, r.lo.y, 1, 8);
+    hi.z = __shfl_down_sync(0xffffffffu, r.lo.z, 1, 8);
+    hi.w = __shfl_down_sync(0xffffffffu, r.lo.w, 1, 8);
+    if (j == 7) hi = r.ex;
+    uint32_t o[4];
+    realign16(r.lo, hi, r.s, o);
+    if (r.nvalid < 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t keep = (2 * i < r.nvalid ? 0x0000FFFFu : 0u) | (2 * i + 1 < r.nvalid ? 0xFFFF0000u : 0u);
+            o[i] &= keep;
+        }
+    }
+    st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+}
+
+template <class Cfg>
+__device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+{
+    constexpr int GROUPS = Cfg::PRODUCER_THREADS / 8;  // row segments per pass
+    constexpr int SEGS = Cfg::BM + Cfg::BK * Cfg::NB64;
+    static_assert(SEGS % GROUPS == 0 && Cfg::BM % GROUPS == 0, "passes split evenly");
+    constexpr int PASSES = SEGS / GROUPS;
+    constexpr int BATCH = 4;
+    static_assert(PASSES % BATCH == 0, "batches");
+
+    const int tid = threadIdx.x;  // producers are threads 0 .. PRODUCER_THREADS-1
+    const int j = tid & 7;
+    const int gslot = tid >> 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t kb_count = 0;
+    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+        const int64_t m0 = (t % p.m_tiles) * Cfg::BM;
+        const int64_t n0 = (t / p.m_tiles) * Cfg::BN;
+        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+            const int64_t k0 = kb * Cfg::BK;
+            const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
+            const uint32_t sb = sa + Cfg::A_BYTES;
+            bool ok = true;
+#pragma unroll 1
+            for (int b0 = 0; b0 < PASSES; b0 += BATCH) {
+                SegLoad ld[BATCH];
+                uint32_t dst[BATCH];
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) {
+                    const int sg = (b0 + u) * GROUPS + gslot;
+                    if (sg < Cfg::BM) {
+                        const int64_t row = m0 + sg;
+                        const bool rv = row < p.M;
+                        ld[u] = seg_issue(rv ? p.A + row * p.lda : p.A, rv, k0, p.K, j);
+                        dst[u] = sa + sg * 128 + ((j ^ (sg & 7)) << 4);
+                    } else {
+                        const int gb = sg - Cfg::BM;
+                        const int kk = gb / Cfg::NB64, jc = gb % Cfg::NB64;
+                        const int64_t row = k0 + kk;
+                        const bool rv = row < p.K;
+                        ld[u] = seg_issue(rv ? p.B + row * p.ldb : p.B, rv, n0 + 64 * jc, p.N, j);
+                        dst[u] = sb + jc * 8192 + kk * 128 + ((j ^ (kk & 7)) << 4);
+                    }
+                }
+                if (b0 == 0) {
+                    // The stage must be free before the first store into it.
+                    const bool got = w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u);
+                    ok = __all_sync(0xffffffffu, got);
+                    if (!ok) break;
+                }
+#pragma unroll
+                for (int u = 0; u < BATCH; ++u) seg_store(ld[u], j, dst[u]);
+            }
+            if (!ok) return;
+            fence_proxy_async_smem();
+            if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) mbar_arrive(smem_u32(&ctl->full[stage]));
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- MMA issuer
+
+template <class Cfg>
+__device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
+                           Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+{
+    constexpr uint32_t IDESC = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
+    bool issued = false, ok = true;
+    for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+        for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
+            const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
+            if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d = tmem_base + acc * Cfg::BN;
+            for (int64_t kb = kc; kb < kend; ++kb) {
+                if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
+                const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
+                    const uint64_t da = umma_desc_sw128(sa + kk * 32, 16, 1024);
+                    const uint64_t db = umma_desc_sw128(sb + kk * 2048, 8192, 1024);
+                    umma_f16(d, da, db, IDESC, (kb > kc || kk > 0) ? 1u : 0u);
+                }
+                issued = true;
+                umma_commit(smem_u32(&ctl->empty[stage]));
+                if (++stage == Cfg::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(smem_u32(&ctl->tfull[acc]));
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    if (!ok && issued) {
+        // Every MMA this thread issued must finish before TMEM is freed.
+        umma_commit(smem_u32(&ctl->drain));
+        w.wait_drain(smem_u32(&ctl->drain), 0, kDrainNs);
+    }
+}
+
+// --------------------------------------------------------------- epilogue
+
+// Stores a 32 x 32 block of 32-bit results: lane l holds row row0 + l,
+// columns col0 .. col0 + 31.  The block goes through the warp's staging tile
+// (16-byte chunks XOR-swizzled by row, conflict-free both ways) so that each
+// global store instruction writes whole 128-byte row pieces.
+__device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, const uint32_t *r,
+                                            int64_t row0, int64_t col0, int lane)
+{
+    if (row0 >= p.M || col0 >= p.N) return;  // warp-uniform
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                     r[4 * c + 3]);
+    __syncwarp();
+    uint32_t *C = static_cast<uint32_t *>(p.C);
+    if (p.vec_store) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3), c = lane & 7;
+            const uint4 v = ld_shared_v4(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+            const int64_t grow = row0 + rr, gcol = col0 + 4 * c;
+            if (grow < p.M && gcol < p.N) {
+                uint32_t *dst = C + grow * p.ldc + gcol;
+                if (gcol + 4 <= p.N) {
+                    *reinterpret_cast<uint4 *>(dst) = v;
+                } else {
+                    dst[0] = v.x;
+                    if (gcol + 1 < p.N) dst[1] = v.y;
+                    if (gcol + 2 < p.N) dst[2] = v.z;
+                }
+            }
+        }
+    } else {
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+            const uint32_t v = ld_shared_b32(stg + rr * 128 + ((((lane >> 2) ^ (rr & 7))) << 4) + ((lane & 3) << 2));
+            const int64_t grow = row0 + rr, gcol = col0 + lane;
+            if (grow < p.M && gcol < p.N) C[grow * p.ldc + gcol] = v;
+        }
+    }
+    __syncwarp();
+}
+
+template <class Cfg>
+__device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES> *ctl,
+                         const Waiter &w, int warp, int lane)
+{
+    const int e = warp - Cfg::EPI_WARP0;  // 0..7
+    const int q = warp & 3;                // TMEM lane quarter this warp may access
+    const int h = e >> 2;                  // column half of the tile
+    const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+        const int64_t row0 = (t % p.m_tiles) * Cfg::BM + q * 32;
+        const int64_t colb = (t / p.m_tiles) * Cfg::BN + h * Cfg::EPI_COLS;
+        uint32_t isum[Cfg::INT_OUT ? Cfg::EPI_COLS : 1];
+        if constexpr (Cfg::INT_OUT) {
+#pragma unroll
+            for (int i = 0; i < Cfg::EPI_COLS; ++i) isum[i] = 0;
+        }
+        for (int64_t kc = 0; kc < p.num_kb; kc += p.kb_per_chunk) {
+            const bool got = w.wait(smem_u32(&ctl->tfull[acc]), acc_phase);
+            if (!__all_sync(0xffffffffu, got)) return;
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * Cfg::EPI_COLS;
+#pragma unroll
+            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                tmem_wait_ld();
+                if constexpr (Cfg::INT_OUT) {
+                    // Chunk partials are integers below 2^24 in magnitude:
+                    // exact in fp32, so the conversion is exact.
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        isum[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+                } else {
+                    store_block(p, stg, r, row0, colb + jb * 32, lane);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if constexpr (Cfg::INT_OUT) {
+#pragma unroll
+            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_pipelined_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const GemmParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    auto *ctl = reinterpret_cast<Ctl<Cfg::STAGES> *>(smem + Cfg::CTL_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), Cfg::LDG ? Cfg::PRODUCER_THREADS : 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->tfull[b]), 1);
+            mbar_init(smem_u32(&ctl->tempty[b]), Cfg::EPI_WARPS);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == Cfg::MMA_WARP) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if constexpr (!Cfg::LDG) {
+        if (threadIdx.x == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const Waiter w{&ctl->abort, p.status, p.timeout_ns};
+
+    if (warp < Cfg::PRODUCER_WARPS) {
+        if constexpr (Cfg::LDG) {
+            producer_ldg<Cfg>(p, sbase, ctl, w);
+        } else {
+            if (lane == 0) producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
+        }
+    } else if (warp == Cfg::MMA_WARP) {
+        if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+        __syncwarp();
+    } else {
+        epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == Cfg::MMA_WARP) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gp

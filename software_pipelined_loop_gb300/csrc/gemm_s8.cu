@@ -1,0 +1,17 @@
+// gemm_s8.cu -- INT8 variants: fp16-widened operands, chunked exact int32 epilogue.
+#include "launch_impl.cuh"
+
+namespace gp {
+
+static const Variant kS8Variants[] = {
+    make_variant<GemmCfg<256, 4, false, true>>(),
+    make_variant<GemmCfg<128, 6, false, true>>(),
+};
+
+int variants_s8(const Variant **out)
+{
+    *out = kS8Variants;
+    return static_cast<int>(sizeof(kS8Variants) / sizeof(kS8Variants[0]));
+}
+
+}  // namespace gp

@@ -1,0 +1,577 @@
+// gemmpipe_api.cpp -- the C ABI declared in include/gemmpipe.h: argument
+// checks, plan selection, tensor-map encoding, the INT8 workspace, kernel
+// timing and the device status word.
+#include "gemmpipe.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "variants.h"
+
+namespace {
+
+using gp::GemmParams;
+using gp::Variant;
+
+constexpr int64_t kMaxDim = 2147483647;  // 2^31 - 1
+constexpr int kBM = 128, kBK = 64;
+constexpr int64_t kInt8ChunkK = 1024;  // k values per exact fp32 partial (1024 * 2^14 = 2^24)
+
+std::mutex g_mu;
+std::atomic<int64_t> g_launches{0};
+
+// ------------------------------------------------------------- device info
+
+struct DeviceInfo {
+    int ok = 0;
+    int major = 0, minor = 0;
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+gemmpipe_status_t device_info(DeviceInfo *out, int *dev_out)
+{
+    static DeviceInfo cache[128];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = cache[dev];
+    if (!d.ok) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
+        }
+        d.ok = 1;
+    }
+    if (d.major != 10 || d.minor != 3) return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
+    *out = d;
+    if (dev_out) *dev_out = dev;
+    return GEMMPIPE_OK;
+}
+
+// -------------------------------------------------------- argument checks
+
+gemmpipe_status_t check_pointer(const void *p, int align)
+{
+    if (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(align)) return GEMMPIPE_ERR_INVALID_VALUE;
+    cudaPointerAttributes a;
+    std::memset(&a, 0, sizeof(a));
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_INVALID_VALUE;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return GEMMPIPE_ERR_INVALID_VALUE;
+    return GEMMPIPE_OK;
+}
+
+// Checks that need no GPU (sizes, null pointers, element alignment).
+gemmpipe_status_t check_shape(int64_t M, int64_t N, int64_t K, const void *A, const void *B, const void *C,
+                              int ab_bytes, int c_bytes)
+{
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMMPIPE_OK;
+    if (!C) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (K > 0 && (!A || !B)) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(C) % c_bytes) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) % ab_bytes) || (reinterpret_cast<uintptr_t>(B) % ab_bytes)))
+        return GEMMPIPE_ERR_INVALID_VALUE;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t check_device_pointers(int64_t K, const void *A, const void *B, const void *C, int ab_bytes,
+                                        int c_bytes)
+{
+    gemmpipe_status_t s = check_pointer(C, c_bytes);
+    if (s != GEMMPIPE_OK) return s;
+    if (K > 0) {
+        if ((s = check_pointer(A, ab_bytes)) != GEMMPIPE_OK) return s;
+        if ((s = check_pointer(B, ab_bytes)) != GEMMPIPE_OK) return s;
+    }
+    return GEMMPIPE_OK;
+}
+
+// ------------------------------------------------------------------ plans
+
+struct Override {
+    int producer = -1, bn = 0, stages = 0;
+};
+Override g_override;
+
+struct StallHook {
+    int64_t kb = -1;
+    int timeout_ms = 0;
+};
+StallHook g_stall;
+
+struct Plan {
+    const Variant *v = nullptr;
+    int grid = 0;
+    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0;
+    int vec_store = 0;
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+const Variant *find_variant(int int_out, int producer, int bn, int stages)
+{
+    const Variant *tab = nullptr;
+    const int n = int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
+    for (int i = 0; i < n; ++i) {
+        const gp::VariantInfo &f = tab[i].info;
+        if (f.producer == producer && f.BN == bn && (stages == 0 || f.stages == stages)) return &tab[i];
+    }
+    return nullptr;
+}
+
+// The plan for an fp16-operand GEMM (INT8 calls pass their widened copies).
+gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                            const void *B, int64_t ldb, const void *C, int64_t ldc, const DeviceInfo &d, Plan *pl)
+{
+    Override ov;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ov = g_override;
+    }
+    const bool tma_ok = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
+    int producer = tma_ok ? 0 : 1;
+    if (ov.producer == 1) producer = 1;
+    if (int_out) producer = 0;  // widened operands are always TMA-describable
+    int bn = N <= 128 ? 128 : 256;
+    if (ov.bn) bn = ov.bn;
+    const Variant *v = find_variant(int_out, producer, bn, ov.stages);
+    if (!v) v = find_variant(int_out, producer, bn, 0);
+    if (!v) return GEMMPIPE_ERR_INTERNAL;
+    if (v->info.smem_bytes > d.smem_optin) return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
+    pl->v = v;
+    pl->m_tiles = (M + kBM - 1) / kBM;
+    pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
+    pl->num_kb = (K + kBK - 1) / kBK;
+    pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
+    pl->grid = static_cast<int>(pl->tiles < d.sms ? pl->tiles : d.sms);
+    pl->vec_store = aligned16(C) && (ldc * 4) % 16 == 0;
+    return GEMMPIPE_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn()
+{
+    static std::atomic<EncodeFn> fn{nullptr};
+    EncodeFn f = fn.load();
+    if (!f) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        f = reinterpret_cast<EncodeFn>(p);
+        fn.store(f);
+    }
+    return f;
+}
+
+// 2-D fp16 tensor (rows x cols, pitch `ld` elements), 128-byte swizzle,
+// box = 64 columns x box_rows rows, zero fill outside the tensor.
+bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+{
+    EncodeFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ timing
+
+struct Timing {
+    bool enabled = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> gemm, aux;
+    std::vector<cudaEvent_t> pool;
+};
+Timing g_timing;
+
+cudaEvent_t take_event()
+{
+    if (!g_timing.pool.empty()) {
+        cudaEvent_t e = g_timing.pool.back();
+        g_timing.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return e;
+}
+
+struct TimedRegion {
+    bool on = false;
+    bool is_gemm;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr, b = nullptr;
+    TimedRegion(bool gemm, cudaStream_t st) : is_gemm(gemm), s(st)
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_timing.enabled) return;
+        a = take_event();
+        b = take_event();
+        if (a && b && cudaEventRecord(a, s) == cudaSuccess) on = true;
+    }
+    void end()
+    {
+        if (!on) return;
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (cudaEventRecord(b, s) == cudaSuccess) (is_gemm ? g_timing.gemm : g_timing.aux).push_back({a, b});
+        on = false;
+    }
+};
+
+// -------------------------------------------------------------- workspace
+
+struct Workspace {
+    void *ptr = nullptr;
+    int64_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+gemmpipe_status_t workspace(int dev, cudaStream_t s, int64_t bytes, void **out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace &w = g_ws[{dev, s}];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            cudaFree(w.ptr);  // synchronizes: earlier users of the buffer have finished
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        if (cudaMalloc(&w.ptr, static_cast<size_t>(bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            w.ptr = nullptr;
+            return GEMMPIPE_ERR_OUT_OF_MEMORY;
+        }
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return GEMMPIPE_OK;
+}
+
+// ------------------------------------------------------------------- runs
+
+gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, int64_t K, const uint16_t *A,
+                           int64_t lda, const uint16_t *B, int64_t ldb, void *C, int64_t ldc, cudaStream_t s)
+{
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (pl.v->info.producer == 0) {
+        if (!encode_2d(&ta, A, M, K, lda, kBM) || !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
+    }
+    GemmParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.A = A;
+    p.lda = lda;
+    p.B = B;
+    p.ldb = ldb;
+    p.C = C;
+    p.ldc = ldc;
+    p.m_tiles = pl.m_tiles;
+    p.tiles = pl.tiles;
+    p.num_kb = pl.num_kb;
+    p.kb_per_chunk = pl.kb_per_chunk;
+    p.vec_store = pl.vec_store;
+    p.stall_kb = -1;
+    p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_stall.kb >= 0) {
+            p.stall_kb = g_stall.kb;
+            p.timeout_ns = static_cast<uint64_t>(g_stall.timeout_ms) * 1000000ull;
+            g_stall = StallHook();
+        }
+    }
+    if (gp::status_word(&p.status) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    TimedRegion tr(true, s);
+    const cudaError_t e = pl.v->launch(ta, tb, p, pl.grid, s);
+    tr.end();
+    if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    (void)int_out;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t zero_c(void *C, int64_t bytes, const DeviceInfo &d, cudaStream_t s)
+{
+    TimedRegion tr(false, s);
+    const cudaError_t e = gp::launch_zero_fill(C, bytes, d.sms, s);
+    tr.end();
+    if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    return GEMMPIPE_OK;
+}
+
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+int64_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return 2 * (M * round8(K) + K * round8(N)); }
+
+}  // namespace
+
+extern "C" {
+
+gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_half_t *A, const gemmpipe_half_t *B,
+                              float *C, gemmpipe_stream_t stream)
+{
+    gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 2, 4);
+    if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
+    DeviceInfo d;
+    if ((st = device_info(&d, nullptr)) != GEMMPIPE_OK) return st;
+    if ((st = check_device_pointers(K, A, B, C, 2, 4)) != GEMMPIPE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, M * N * 4, d, s);
+    Plan pl;
+    if ((st = make_plan(false, M, N, K, A, K, B, N, C, N, d, &pl)) != GEMMPIPE_OK) return st;
+    return run_plan(pl, false, M, N, K, A, K, B, N, C, N, s);
+}
+
+gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B, int32_t *C,
+                               gemmpipe_stream_t stream)
+{
+    gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 1, 4);
+    if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceInfo d;
+    if ((st = device_info(&d, &dev)) != GEMMPIPE_OK) return st;
+    if ((st = check_device_pointers(K, A, B, C, 1, 4)) != GEMMPIPE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, M * N * 4, d, s);
+    const int64_t Kp = round8(K), Np = round8(N);
+    void *ws = nullptr;
+    if ((st = workspace(dev, s, s8_workspace_bytes(M, N, K), &ws)) != GEMMPIPE_OK) return st;
+    uint16_t *A16 = static_cast<uint16_t *>(ws);
+    uint16_t *B16 = A16 + M * Kp;
+    {
+        TimedRegion tr(false, s);
+        const cudaError_t e = gp::launch_widen_s8_f16(A, M, K, A16, Kp, B, K, N, B16, Np, d.sms, s);
+        tr.end();
+        if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+        g_launches.fetch_add(1);
+    }
+    Plan pl;
+    if ((st = make_plan(true, M, N, K, A16, Kp, B16, Np, C, N, d, &pl)) != GEMMPIPE_OK) return st;
+    return run_plan(pl, true, M, N, K, A16, Kp, B16, Np, C, N, s);
+}
+
+gemmpipe_status_t gemmpipe_get_device_status(gemmpipe_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    int *w = nullptr;
+    if (gp::status_word(&w) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    int v = 0;
+    if (cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    }
+    if (v == GEMMPIPE_ERR_TIMEOUT) return GEMMPIPE_ERR_TIMEOUT;
+    if (v != 0) return GEMMPIPE_ERR_INTERNAL;
+    return GEMMPIPE_OK;
+}
+
+const char *gemmpipe_status_string(gemmpipe_status_t status)
+{
+    switch (status) {
+    case GEMMPIPE_OK: return "ok";
+    case GEMMPIPE_ERR_INVALID_VALUE: return "invalid value";
+    case GEMMPIPE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case GEMMPIPE_ERR_LAUNCH: return "kernel launch or CUDA runtime error";
+    case GEMMPIPE_ERR_TIMEOUT: return "a pipeline wait on the device ran out of time";
+    case GEMMPIPE_ERR_INTERNAL: return "internal error";
+    case GEMMPIPE_ERR_OUT_OF_MEMORY: return "out of device memory";
+    }
+    return "unknown status";
+}
+
+double gemmpipe_compute_load_ratio(int BM, int BN, int BK, int elem_bytes)
+{
+    if (BM < 1 || BN < 1 || BK < 1 || elem_bytes < 1) return -1.0;
+    const double mac_flops = 2.0 * BM * static_cast<double>(BN) * BK;
+    const double tile_bytes = (static_cast<double>(BM) * BK + static_cast<double>(BK) * BN) * elem_bytes;
+    return mac_flops / tile_bytes;
+}
+
+int64_t gemmpipe_stage_smem_bytes(int BM, int BN, int BK, int elem_bytes, int stages)
+{
+    if (BM < 1 || BN < 1 || BK < 1 || elem_bytes < 1 || stages < 1) return -1;
+    return static_cast<int64_t>(stages) * (static_cast<int64_t>(BM) * BK + static_cast<int64_t>(BK) * BN) *
+           elem_bytes;
+}
+
+gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                                const void *C, gemmpipe_plan_t *plan)
+{
+    if (!plan || (dtype != 0 && dtype != 1)) return GEMMPIPE_ERR_INVALID_VALUE;
+    const bool s8 = dtype == 0;
+    gemmpipe_status_t st = check_shape(M, N, K, A, B, C, s8 ? 1 : 2, 4);
+    if (st != GEMMPIPE_OK) return st;
+    DeviceInfo d;
+    if ((st = device_info(&d, nullptr)) != GEMMPIPE_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    if (M == 0 || N == 0 || K == 0) return GEMMPIPE_OK;
+    Plan pl;
+    if (s8) {
+        // The widened copies are 16-byte aligned with 16-byte row pitches.
+        static const uint16_t *const kAligned = reinterpret_cast<const uint16_t *>(256);
+        st = make_plan(true, M, N, K, kAligned, round8(K), kAligned, round8(N), C, N, d, &pl);
+    } else {
+        st = make_plan(false, M, N, K, A, K, B, N, C, N, d, &pl);
+    }
+    if (st != GEMMPIPE_OK) return st;
+    const gp::VariantInfo &f = pl.v->info;
+    plan->producer = f.producer;
+    plan->BM = f.BM;
+    plan->BN = f.BN;
+    plan->BK = f.BK;
+    plan->stages = f.stages;
+    plan->k_chunk = static_cast<int>(pl.kb_per_chunk * f.BK < K ? pl.kb_per_chunk * f.BK : K);
+    plan->threads = f.threads;
+    plan->grid = pl.grid;
+    plan->tiles = pl.tiles;
+    plan->k_blocks = pl.num_kb;
+    plan->smem_bytes = f.smem_bytes;
+    plan->vector_store = pl.vec_store;
+    plan->workspace_bytes = s8 ? s8_workspace_bytes(M, N, K) : 0;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages)
+{
+    if (producer < -1 || producer > 1) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_override.producer = producer;
+    g_override.bn = bn;
+    g_override.stages = stages;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_release_workspaces(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    const bool have = cudaGetDevice(&cur) == cudaSuccess;
+    for (auto &kv : g_ws) {
+        if (kv.second.ptr) {
+            cudaSetDevice(kv.first.first);
+            cudaFree(kv.second.ptr);
+        }
+    }
+    g_ws.clear();
+    if (have) cudaSetDevice(cur);
+    cudaGetLastError();
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_timing_enable(int enable)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_timing.enabled = enable != 0;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_timing_read(double *gemm_ms, int64_t *gemm_launches, double *aux_ms,
+                                       int64_t *aux_launches)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    gemmpipe_status_t st = GEMMPIPE_OK;
+    auto sum = [&](std::vector<std::pair<cudaEvent_t, cudaEvent_t>> &v, double *ms, int64_t *n) {
+        double t = 0.0;
+        for (auto &pr : v) {
+            float f = 0.f;
+            if (cudaEventSynchronize(pr.second) != cudaSuccess ||
+                cudaEventElapsedTime(&f, pr.first, pr.second) != cudaSuccess) {
+                cudaGetLastError();
+                st = GEMMPIPE_ERR_LAUNCH;
+            }
+            t += f;
+            g_timing.pool.push_back(pr.first);
+            g_timing.pool.push_back(pr.second);
+        }
+        if (ms) *ms = t;
+        if (n) *n = static_cast<int64_t>(v.size());
+        v.clear();
+    };
+    sum(g_timing.gemm, gemm_ms, gemm_launches);
+    sum(g_timing.aux, aux_ms, aux_launches);
+    return st;
+}
+
+int64_t gemmpipe_launch_count(void) { return g_launches.load(); }
+
+gemmpipe_status_t gemmpipe_copy(void *dst, const void *src, int64_t bytes, gemmpipe_stream_t stream)
+{
+    if (bytes < 0) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (bytes == 0) return GEMMPIPE_OK;
+    if (!dst || !src) return GEMMPIPE_ERR_INVALID_VALUE;
+    DeviceInfo d;
+    gemmpipe_status_t st = device_info(&d, nullptr);
+    if (st != GEMMPIPE_OK) return st;
+    if ((st = check_pointer(dst, 1)) != GEMMPIPE_OK || (st = check_pointer(src, 1)) != GEMMPIPE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    TimedRegion tr(false, s);
+    const cudaError_t e = gp::launch_copy(dst, src, bytes, d.sms, s);
+    tr.end();
+    if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int timeout_ms)
+{
+    if (k_block >= 0 && (timeout_ms < 1 || timeout_ms > 60000)) return GEMMPIPE_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_stall.kb = k_block < 0 ? -1 : k_block;
+    g_stall.timeout_ms = timeout_ms;
+    return GEMMPIPE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// variants.h -- host-side table of the compiled kernel variants.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gemm_params.h"
+
+namespace gp {
+
+struct VariantInfo {
+    int producer;  // 0 TMA, 1 bounded loads
+    int int_out;   // 1: INT8 chunked integer epilogue
+    int BM, BN, BK, stages;
+    int threads;
+    int smem_bytes;
+};
+
+using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const GemmParams &, int grid,
+                                 cudaStream_t);
+
+struct Variant {
+    VariantInfo info;
+    LaunchFn launch;
+};
+
+// Each kernel translation unit exports its variants.
+int variants_f16(const Variant **out);
+int variants_s8(const Variant **out);
+
+// Auxiliary kernels (aux_kernels.cu).
+cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16, int64_t pitchA16,
+                                const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB16,
+                                int sms, cudaStream_t s);
+cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s);
+cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s);
+cudaError_t status_word(int **ptr);  // device address of the current device's status word
+
+}  // namespace gp

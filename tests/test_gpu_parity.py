@@ -1,0 +1,309 @@
+"""GPU parity: the CUDA library through the C ABI against the CPU oracle.
+
+INT8 results must equal the oracle bit for bit.  FP16 results (fp32
+accumulation on the tensor cores) must be within max-abs 1e-2 and relative
+Frobenius 1e-4 of the oracle's fp64-accumulated product.
+
+Sizes the oracle finishes in seconds are compared element by element; the
+full-size workloads are compared on sampled rows (every column of each
+sampled row, so every column tile including the ragged last one), chosen to
+include the first and last rows of M tiles.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from software_pipelined_loop_gb300 import gemmpipe, inputs
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+MAX_REL_FRO = 1e-4
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from software_pipelined_loop_gb300 import build
+    build.build()
+    gemmpipe.load()
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    yield torch.device("cuda:0")
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+
+
+def to_dev(a: np.ndarray, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def run_f16(A: np.ndarray, B: np.ndarray, dev) -> np.ndarray:
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    gemmpipe.gemm_f16f32(M, N, K, to_dev(A, dev), to_dev(B, dev), C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    return C.cpu().numpy()
+
+
+def run_s8(A: np.ndarray, B: np.ndarray, dev) -> np.ndarray:
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    C = torch.full((M, N), -7, dtype=torch.int32, device=dev)
+    gemmpipe.gemm_s8s8s32(M, N, K, to_dev(A, dev), to_dev(B, dev), C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    return C.cpu().numpy()
+
+
+def assert_f16_close(got: np.ndarray, ref: np.ndarray, what=""):
+    assert got.shape == ref.shape
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    d = got.astype(np.float64) - ref.astype(np.float64)
+    err = np.abs(d).max() if d.size else 0.0
+    nrm = np.linalg.norm(ref.astype(np.float64))
+    rel = np.linalg.norm(d) / nrm if nrm > 0 else np.linalg.norm(d)
+    assert err <= MAX_ABS and rel <= MAX_REL_FRO, f"{what}: max-abs {err:.3g} rel-fro {rel:.3g}"
+
+
+def sample_rows(M: int, n_random: int = 24, seed: int = 7) -> np.ndarray:
+    fixed = {0, 1, 63, 64, 127, 128, 129, 255, 256, M // 2, M - 129, M - 128, M - 2, M - 1}
+    rng = np.random.default_rng(seed)
+    rnd = set(int(x) for x in rng.integers(0, M, n_random))
+    return np.array(sorted(r for r in fixed | rnd if 0 <= r < M), dtype=np.int64)
+
+
+# --------------------------------------------------------------- small sweeps
+
+SWEEP = [
+    # (M, N, K): aligned pitches (TMA producer) and odd ones (bounded loads)
+    (1, 8, 8), (1, 1, 1), (17, 24, 64), (128, 128, 64), (129, 136, 72), (300, 264, 192),
+    (128, 256, 128), (255, 512, 1000), (64, 8, 4096), (129, 129, 129), (15, 17, 127),
+    (16, 16, 16), (127, 1, 65), (200, 300, 17), (33, 513, 250), (300, 7, 1031),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SWEEP)
+def test_f16_sweep(dev, M, N, K):
+    A, B = inputs.make_operands("f16", M, N, K, seed=100 + M + 7 * N + 13 * K)
+    assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", SWEEP)
+def test_s8_sweep(dev, M, N, K):
+    A, B = inputs.make_operands("s8", M, N, K, seed=200 + M + 7 * N + 13 * K)
+    assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+
+
+# The page's pitfalls (last K tile dropped, off-by-one in the buffer index):
+# number of k-blocks around the ring depth S (4 for 128x256 tiles, 6 for
+# 128x128), including the last tile being a partial one.
+@pytest.mark.parametrize("num_kb", [1, 2, 3, 4, 5, 6, 7, 9, 13])
+@pytest.mark.parametrize("N", [128, 256])
+def test_ring_depth_edges(dev, num_kb, N):
+    for K in (64 * num_kb, 64 * num_kb - 24):
+        A, B = inputs.make_operands("f16", 256, N, K, seed=300 + num_kb + K)
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), f"K={K}")
+
+
+@pytest.mark.parametrize("producer", [0, 1])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_forced_producer_and_tile(dev, producer, bn):
+    M, N, K = 384, 520, 704
+    A, B = inputs.make_operands("f16", M, N, K, seed=400 + bn + producer)
+    gemmpipe.gemmpipe_set_plan_override(producer, bn, 0)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert plan["producer"] == producer and plan["BN"] == bn
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert_f16_close(got, oracle.gemm_f16f32(A, B))
+
+
+def test_misaligned_base_pointers(dev):
+    import torch
+    # A and B start 2 bytes past a 16-byte boundary, C 4 bytes past: the
+    # bounded-load producer and 4-byte stores must take over.
+    M, N, K = 200, 136, 264
+    A, B = inputs.make_operands("f16", M, N, K, seed=11)
+    ab = torch.zeros(M * K + 8, dtype=torch.float16, device=dev)
+    bb = torch.zeros(K * N + 8, dtype=torch.float16, device=dev)
+    cb = torch.zeros(M * N + 4, dtype=torch.float32, device=dev)
+    ab[1:1 + M * K] = to_dev(A.reshape(-1), dev)
+    bb[1:1 + K * N] = to_dev(B.reshape(-1), dev)
+    a_ptr, b_ptr, c_ptr = ab.data_ptr() + 2, bb.data_ptr() + 2, cb.data_ptr() + 4
+    plan = gemmpipe.gemmpipe_plan(1, M, N, K, a_ptr, b_ptr, c_ptr)
+    assert plan["producer"] == 1 and plan["vector_store"] == 0
+    gemmpipe.gemm_f16f32(M, N, K, a_ptr, b_ptr, c_ptr)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    got = cb[1:1 + M * N].cpu().numpy().reshape(M, N)
+    assert_f16_close(got, oracle.gemm_f16f32(A, B))
+    assert cb[0].item() == 0 and cb[M * N + 1:].abs().sum().item() == 0
+
+
+def test_guard_bands_untouched(dev):
+    import torch
+    M, N, K = 257, 264, 128
+    A, B = inputs.make_operands("f16", M, N, K, seed=12)
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 12345.0, dtype=torch.float32, device=dev)
+    c_ptr = buf.data_ptr() + 4 * pad
+    gemmpipe.gemm_f16f32(M, N, K, to_dev(A, dev), to_dev(B, dev), c_ptr)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    host = buf.cpu().numpy()
+    assert (host[:pad] == 12345.0).all() and (host[pad + M * N:] == 12345.0).all()
+    assert_f16_close(host[pad:pad + M * N].reshape(M, N), oracle.gemm_f16f32(A, B))
+
+
+def test_empty_shapes(dev):
+    import torch
+    C = torch.full((5, 9), 3.0, dtype=torch.float32, device=dev)
+    A = torch.zeros((5, 0), dtype=torch.float16, device=dev)
+    B = torch.zeros((0, 9), dtype=torch.float16, device=dev)
+    gemmpipe.gemm_f16f32(5, 9, 0, A, B, C)           # empty sum: zeros
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert (C == 0).all()
+    Ci = torch.full((5, 9), 3, dtype=torch.int32, device=dev)
+    gemmpipe.gemm_s8s8s32(5, 9, 0, A.to(torch.int8), B.to(torch.int8), Ci)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert (Ci == 0).all()
+    gemmpipe.gemm_f16f32(0, 9, 4, None, None, None)   # nothing to do
+    gemmpipe.gemm_s8s8s32(5, 0, 4, None, None, None)
+
+
+def test_host_pointer_rejected(dev):
+    import torch
+    A = torch.zeros((8, 8), dtype=torch.float16)      # host memory
+    B = torch.zeros((8, 8), dtype=torch.float16, device=dev)
+    C = torch.zeros((8, 8), dtype=torch.float32, device=dev)
+    with pytest.raises(gemmpipe.GemmpipeError) as ei:
+        gemmpipe.gemm_f16f32(8, 8, 8, A, B, C)
+    assert ei.value.status == gemmpipe.ERR_INVALID_VALUE
+
+
+# ----------------------------------------------------------- INT8 exactness
+
+@pytest.mark.parametrize("K", [1024, 1025, 2048, 3000, 4096])
+def test_s8_chunk_exactness_extremes(dev, K):
+    # Products of +-127/-128 make every chunk partial an odd or large integer
+    # near 2^24 in magnitude: any bit the fp32 accumulation dropped shows.
+    M, N = 130, 264
+    rng = np.random.default_rng(K)
+    A = rng.choice(np.array([-128, 127, -127], dtype=np.int8), size=(M, K))
+    B = rng.choice(np.array([-128, 127, 127], dtype=np.int8), size=(K, N))
+    A[0, :] = 127
+    B[:, 0] = 127          # C[0,0] = 16129 K: odd partials just below 2^24
+    A[1, :] = -128
+    B[:, 1] = -128         # C[1,1] = 16384 K: the chunk bound itself
+    got = run_s8(A, B, dev)
+    want = oracle.gemm_s8s8s32(A, B)
+    assert np.array_equal(got, want)
+    assert got[0, 0] == 16129 * K and got[1, 1] == 16384 * K
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_workload_int8_512(dev):
+    _, _, M, N, K, A, B = inputs.workload_operands(0)
+    assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+
+
+def test_workload_fp16_1024(dev):
+    _, _, M, N, K, A, B = inputs.workload_operands(1)
+    assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), "fp16 1024^3")
+
+
+def test_workload_int8_4096_sampled(dev):
+    _, _, M, N, K, A, B = inputs.workload_operands(2)
+    got = run_s8(A, B, dev)
+    rows = sample_rows(M)
+    assert np.array_equal(got[rows], oracle.gemm_s8s8s32(A, B, rows=rows))
+    # Any-size property: int8 products are bounded by 2^14 K.
+    assert np.abs(got.astype(np.int64)).max() <= 16384 * K
+
+
+def test_workload_fp16_skinny_sampled(dev):
+    _, _, M, N, K, A, B = inputs.workload_operands(3)
+    got = run_f16(A, B, dev)
+    rows = sample_rows(M)
+    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "skinny")
+    assert np.isfinite(got).all()
+
+
+def test_workload_fp16_ragged_sampled(dev):
+    _, _, M, N, K, A, B = inputs.workload_operands(4)
+    plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+    got = run_f16(A, B, dev)
+    rows = sample_rows(M)
+    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "ragged")
+    assert np.isfinite(got).all()
+    assert plan["k_blocks"] == (K + 63) // 64
+
+
+# --------------------------------------------------------- bounded waits
+
+def test_stall_times_out_and_context_survives(dev):
+    import torch
+    M, N, K = 256, 256, 1024
+    A, B = inputs.make_operands("f16", M, N, K, seed=13)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    gemmpipe.gemmpipe_test_inject_stall(3, 200)
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+    # The context is still usable and the hook was one-shot.
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
+
+
+def test_stall_times_out_bounded_load_producer(dev):
+    import torch
+    M, N, K = 129, 200, 333   # odd pitches: bounded-load producer
+    A, B = inputs.make_operands("f16", M, N, K, seed=14)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    gemmpipe.gemmpipe_test_inject_stall(1, 200)
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
+
+
+def test_kernel_timing_and_launch_count(dev):
+    import torch
+    M = N = K = 512
+    A, B = inputs.make_operands("s8", M, N, K, seed=15)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.int32, device=dev)
+    n0 = gemmpipe.gemmpipe_launch_count()
+    gemmpipe.gemmpipe_timing_enable(True)
+    try:
+        for _ in range(3):
+            gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C)
+        gms, gn, ams, an = gemmpipe.gemmpipe_timing_read()
+    finally:
+        gemmpipe.gemmpipe_timing_enable(False)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert gn == 3 and an == 3 and gms > 0 and ams > 0
+    assert gemmpipe.gemmpipe_launch_count() - n0 == 6
+
+
+def test_copy_kernel(dev):
+    import torch
+    src = torch.arange(1 << 20, dtype=torch.int32, device=dev)
+    dst = torch.zeros_like(src)
+    gemmpipe.gemmpipe_copy(dst, src, src.numel() * 4)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert torch.equal(src, dst)
+    odd = torch.zeros(1001, dtype=torch.uint8, device=dev)
+    gemmpipe.gemmpipe_copy(odd.data_ptr() + 1, src.data_ptr() + 3, 999)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert torch.equal(odd[1:1000].cpu(), src.cpu().view(torch.uint8)[3:1002])
