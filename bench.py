@@ -1,0 +1,394 @@
+"""Benchmark of libgemmpipe on the named GEMM workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Headline (``value``): INT8 IGEMM M = N = K = 4096 (the pages' benchmark shape),
+int8 operands uniform on [-128, 127], int32 C, in TOPS.  A step is one
+gemm_s8s8s32 call through the C ABI with inputs resident in HBM.  Because the
+inputs (32 MiB) fit in the 126 MiB L2, a 256 MiB buffer is written between
+timed steps and each step is timed alone with CUDA events on its stream.
+
+Also measured in the same run and reported under ``secondary``: FP16
+4096^3 (TFLOPS), the skinny FP16 16384 x 128 x 16384 (GB/s of algorithmic
+bytes: A, B and C moved once) and the ragged FP16 4093 x 3001 x 4107.
+
+``--impl reference`` times the CPU oracle on the host cores instead, on a
+bounded sample of rows of the same workload.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica of
+the workload (the GEMM does not shard across GPUs here); ``value`` is the
+total of all ranks' operations over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT8 TOPS and FP16 TFLOPS at 4096³ (% of dense tensor peak); GB/s on skinny"
+HEADLINE = 2  # index of the INT8 4096^3 workload in inputs.WORKLOADS
+FLUSH_BYTES = 256 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (20 Hz) with host timestamps; the bench asks for
+    the ones that fall inside its timed window."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [s for t, s in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        if not win:
+            win = [s for _, s in self.samples]
+        sm = [float(s[0]) for s in win if s and s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in win if len(s) > 1 and s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4) if len(s) > 4 + i and s[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def workload(index: int):
+    from software_pipelined_loop_gb300 import inputs
+    return inputs.workload_operands(index)
+
+
+def cpu_oracle_rate(A, B, dtype: str, target_s: float, max_rows: int | None = None) -> dict:
+    """Times the oracle on the first rows of the workload for about target_s."""
+    import oracle
+    M, K = A.shape
+    N = B.shape[1]
+    fn = oracle.gemm_s8s8s32 if dtype == "s8" else oracle.gemm_f16f32
+    threads = oracle.default_threads()
+    rows = min(M, max(threads, 8))
+    t = time.perf_counter()
+    fn(A, B, rows=list(range(rows)), threads=threads)
+    dt = time.perf_counter() - t
+    if dt < target_s:
+        rows = int(min(M, max(rows, rows * target_s / max(dt, 1e-3))))
+        if max_rows:
+            rows = min(rows, max_rows)
+        t = time.perf_counter()
+        fn(A, B, rows=list(range(rows)), threads=threads)
+        dt = time.perf_counter() - t
+    ops = 2.0 * rows * N * K
+    return {"value": ops / dt / 1e12, "cores": threads, "seconds": dt, "rows": rows}
+
+
+def run_reference(args) -> int:
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name, dtype, M, N, K, A, B = workload(HEADLINE)
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_rate(A, B, dtype, target_s=0.0, max_rows=8)
+    vals, secs, rows, cores = [], 0.0, 0, 1
+    for _ in range(max(1, args.steps)):
+        r = cpu_oracle_rate(A, B, dtype, target_s=args.ref_seconds)
+        vals.append(r["value"])
+        secs += r["seconds"]
+        rows = r["rows"]
+        cores = r["cores"]
+    v = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": name, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": v, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"first {rows} of {M} rows of C per step (all {N} columns, full K)"},
+        "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def time_steps(call, steps: int, flush=None, stream=None) -> list[float]:
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each."""
+    import torch
+    evs = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def measure_gemm(wl, steps: int, warmup: int, dev, flush, peaks, peak_src):
+    """Device-resident timing of one workload (name, dtype, M, N, K, A, B)."""
+    import torch
+
+    from software_pipelined_loop_gb300 import gemmpipe
+    name, dtype, M, N, K, A, B = wl
+    Ad = torch.from_numpy(A).to(dev)
+    Bd = torch.from_numpy(B).to(dev)
+    C = torch.empty((M, N), dtype=torch.int32 if dtype == "s8" else torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = gemmpipe.gemm_s8s8s32 if dtype == "s8" else gemmpipe.gemm_f16f32
+    call = lambda: fn(M, N, K, Ad, Bd, C, stream)
+    in_bytes = A.nbytes + B.nbytes
+    needs_flush = in_bytes < FLUSH_BYTES
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    st = gemmpipe.gemmpipe_get_device_status(stream)
+    if st != gemmpipe.OK:
+        raise RuntimeError(f"{name}: device status {gemmpipe.STATUS.get(st, st)}")
+    gemmpipe.gemmpipe_timing_read()
+    gemmpipe.gemmpipe_timing_enable(True)
+    launches0 = gemmpipe.gemmpipe_launch_count()
+    t0 = time.time()
+    times = time_steps(call, steps, flush if needs_flush else None, stream)
+    t1 = time.time()
+    launches = gemmpipe.gemmpipe_launch_count() - launches0
+    gemm_ms, gemm_n, aux_ms, aux_n = gemmpipe.gemmpipe_timing_read()
+    gemmpipe.gemmpipe_timing_enable(False)
+    st = gemmpipe.gemmpipe_get_device_status(stream)
+    if st != gemmpipe.OK:
+        raise RuntimeError(f"{name}: device status {gemmpipe.STATUS.get(st, st)}")
+    ms = statistics.mean(times)
+    flops = 2.0 * M * N * K
+    alg_bytes = in_bytes + C.numel() * C.element_size()
+    kernel_ms = gemm_ms / max(1, gemm_n)
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K, Ad, Bd, C)
+    skinny = N <= 128
+    if skinny:
+        peak = peaks["hbm_gbs"]
+        achieved = alg_bytes / kernel_ms / 1e6
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": f"hbm_gbs ({peak_src})"}
+    else:
+        peak = peaks["bf16_tflops"]
+        achieved = flops / kernel_ms / 1e9
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"bf16_tflops burst ({peak_src}); kind::f16 runs at the bf16 rate"}
+    return {
+        "name": name, "dtype": dtype, "M": M, "N": N, "K": K, "ms": ms, "ms_median": statistics.median(times),
+        "ops_per_s": flops / ms / 1e9, "bytes_per_s": alg_bytes / ms / 1e6, "kernel_ms": kernel_ms,
+        "aux_ms": aux_ms / max(1, aux_n) if aux_n else 0.0, "launches": launches, "flops": flops,
+        "alg_bytes": alg_bytes, "roofline": roof, "plan": plan, "l2": "flushed" if needs_flush else "inputs > L2",
+        "window": (t0, t1), "A": A, "B": B,
+    }
+
+
+def measure_e2e(res: dict, steps: int, dev) -> dict:
+    """Same GEMM through the C ABI with host buffers: pinned H2D of A and B,
+    the call, D2H of C, all inside the event-timed region."""
+    import torch
+
+    from software_pipelined_loop_gb300 import gemmpipe
+    A, B, M, N, K = res["A"], res["B"], res["M"], res["N"], res["K"]
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    out_dtype = torch.int32 if res["dtype"] == "s8" else torch.float32
+    Ch = torch.empty((M, N), dtype=out_dtype).pin_memory()
+    Ad = torch.empty_like(Ah, device=dev)
+    Bd = torch.empty_like(Bh, device=dev)
+    Cd = torch.empty((M, N), dtype=out_dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = gemmpipe.gemm_s8s8s32 if res["dtype"] == "s8" else gemmpipe.gemm_f16f32
+
+    def call():
+        Ad.copy_(Ah, non_blocking=True)
+        Bd.copy_(Bh, non_blocking=True)
+        fn(M, N, K, Ad, Bd, Cd, stream)
+        Ch.copy_(Cd, non_blocking=True)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    times = time_steps(call, steps, None, stream)
+    ms = statistics.mean(times)
+    return {"value": res["flops"] / ms / 1e9, "unit": "TOPS" if res["dtype"] == "s8" else "TFLOPS",
+            "ms_per_step": ms, "h2d_bytes_per_step": A.nbytes + B.nbytes,
+            "d2h_bytes_per_step": Ch.numel() * Ch.element_size()}
+
+
+def run_gpu(args) -> int:
+    import torch
+
+    from software_pipelined_loop_gb300 import build, gemmpipe
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    gemmpipe.load()
+    peaks, peak_src = load_peaks()
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+
+    clock = ClockSampler(local)
+    clock.start()
+    try:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        head = measure_gemm(workload(HEADLINE), args.steps, args.warmup, dev, flush, peaks, peak_src)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clocks = clock.summary(*head["window"])
+        if clocks["samples"] < 3:
+            clocks["window"] = "whole GPU phase (timed region shorter than the sampling period)"
+        secondary = {}
+        if not args.no_secondary:
+            for wl in (fp16_4096(), workload(3), workload(4)):
+                r = measure_gemm(wl, max(10, args.steps // 4), args.warmup, dev, flush, peaks, peak_src)
+                secondary[r["name"]] = r
+        e2e = measure_e2e(head, max(5, args.steps // 4), dev)
+    finally:
+        clock.stop()
+
+    ms = head["ms"]
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * head["flops"] / ms / 1e9
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        r = cpu_oracle_rate(head["A"], head["B"], head["dtype"], target_s=args.cpu_seconds)
+        cpu = {"value": r["value"], "unit": "TOPS", "cores": r["cores"], "kind": "oracle",
+               "sample": f"first {r['rows']} of {head['M']} rows of C (all {head['N']} columns, full K), "
+                         f"{r['seconds']:.1f} s"}
+
+    def brief(r):
+        unit = "GB/s" if r["N"] <= 128 else ("TOPS" if r["dtype"] == "s8" else "TFLOPS")
+        val = r["bytes_per_s"] if r["N"] <= 128 else r["ops_per_s"]
+        return {"value": val, "unit": unit, "ms_per_step": r["ms"], "kernel_ms": r["kernel_ms"],
+                "roofline": r["roofline"], "l2": r["l2"],
+                "plan": {k: r["plan"][k] for k in ("producer", "BN", "stages", "grid", "tiles")},
+                "shape": [r["M"], r["N"], r["K"]]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8",
+        "dtype_note": "int8 operands widened to fp16 (exact), tcgen05 kind::f16 with fp32 accumulation "
+                      "in <=1024-k chunks, exact int32 sum",
+        "data": "synthetic",
+        "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
+                   "l2": "256 MiB buffer written between timed steps (inputs 32 MiB < L2)",
+                   "replicas": world},
+        "roofline": head["roofline"],
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": head["launches"],
+        "clocks": clocks,
+        "kernel_ms": head["kernel_ms"], "aux_ms": head["aux_ms"],
+        "secondary": {k: brief(v) for k, v in secondary.items()},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def fp16_4096():
+    """FP16 4096^3, operands uniform on [-1, 1]: the fp16 half of the metric."""
+    from software_pipelined_loop_gb300 import inputs
+    A, B = inputs.make_operands("f16", 4096, 4096, 4096, inputs.SEED_BASE + 5)
+    return ("fp16_4096", "f16", 4096, 4096, 4096, A, B)
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -17,18 +17,24 @@
  *     B: K x N, element (k, j) at B[k*N + j]
  *     C: M x N, element (i, j) at C[i*N + j]
  * C is overwritten (no alpha/beta: the pages define none).  A, B and C must
- * not overlap.  No alignment beyond the element size is required; inputs
- * whose base or row pitch is not a multiple of 16 bytes take a slower
- * producer path (bounds-checked loads instead of the tensor-memory
- * accelerator), with identical results.
+ * not overlap.  No alignment beyond the element size is required.  An fp16
+ * operand whose base or row pitch is not a multiple of 16 bytes cannot be
+ * read by the tensor-memory accelerator (TMA); gemm_f16f32 then copies it
+ * into the library workspace with a padded, aligned pitch ("Pipeline GPU
+ * Kernel", pitfalls list: pad the inputs, or fall back to bounds-checked
+ * loads) and, where that workspace cannot be had or the bounded-load
+ * producer is forced, reads it with bounds-checked loads instead.  Results
+ * are the same either way.
  *
  * Ownership: the caller allocates A, B and C in device memory (cudaMalloc,
  * or managed memory) on the current device and keeps them alive until the
- * work on `stream` has finished.  gemm_f16f32 allocates nothing.
- * gemm_s8s8s32 keeps a library-owned device workspace (the operands widened
- * to fp16, see its comment), allocated on first use with cudaMalloc, grown
- * when a larger problem needs it, one per (device, stream), released by
- * gemmpipe_release_workspaces() or at unload.
+ * work on `stream` has finished.  The library keeps a device workspace per
+ * (device, stream) for operand copies -- gemm_s8s8s32's operands widened to
+ * fp16, and misaligned fp16 operands of gemm_f16f32 padded to aligned rows --
+ * allocated with cudaMalloc on first need, grown when a larger problem needs
+ * it (cudaFree then waits for the device), released by
+ * gemmpipe_release_workspaces() or at unload.  gemm_f16f32 with 16-byte
+ * aligned operands and pitches allocates nothing.
  *
  * Execution: every GEMM call is asynchronous on `stream` (a cudaStream_t;
  * NULL is the legacy default stream) and targets the current CUDA device.
@@ -153,17 +159,22 @@ typedef struct {
     int k_chunk;         /* k values accumulated in one TMEM accumulator before a drain */
     int threads;         /* threads per CTA */
     int grid;            /* persistent CTAs launched */
-    int64_t tiles;       /* output tiles */
+    int64_t tiles;       /* output tiles of BM x BN */
+    int64_t tasks;       /* work items: tiles, with the last partial wave split into BN/2-wide halves */
     int64_t k_blocks;    /* ceil(K / BK) */
     int64_t smem_bytes;  /* dynamic shared memory per CTA */
     int vector_store;    /* 1: 16-byte stores of C, 0: 4-byte stores */
-    int64_t workspace_bytes; /* library workspace the call needs (INT8 only) */
+    int operand_copy;    /* 0: none, 1: int8 widened to fp16, 2: misaligned fp16 padded */
+    int64_t workspace_bytes; /* library workspace the call needs */
 } gemmpipe_plan_t;
 
 /*
  * Fills *plan with the kernel configuration that gemm_s8s8s32 (dtype 0) or
  * gemm_f16f32 (dtype 1) would use for these arguments on the current device.
- * Launches nothing.  Same argument checks as the GEMM calls.
+ * Launches nothing and dereferences no pointer.  A, B or C may be NULL: a
+ * NULL pointer is planned as if it were 256-byte aligned.  Sizes are checked
+ * as in the GEMM calls (INVALID_VALUE); M, N or K equal to 0 give an all-zero
+ * plan.  Needs a compute capability 10.3 device (else UNSUPPORTED_DEVICE).
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K,
                                 const void *A, const void *B, const void *C,

@@ -5,61 +5,143 @@
 
 #include <atomic>
 
+#include "ptx.cuh"
 #include "variants.h"
 
 namespace gp {
 
 __device__ int g_status_word;
 
-// Widen one int8 row segment of up to 16 values into fp16 bit patterns.
-__device__ __forceinline__ void widen16(const int8_t *src, int64_t valid, uint16_t *dst, int64_t room)
+// int8 -> fp16 for four packed bytes.  Biasing each byte by 128 gives
+// u = v + 128 in [0, 255]; the fp16 bit pattern 0x6400 | u is 1024 + u
+// exactly, and subtracting 1152 in fp16 leaves v exactly (integers below
+// 2048 are representable).  Returns the halves of bytes 0,1 and 2,3.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    uint16_t h[16];
-    if (valid >= 16 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int8_t b = static_cast<int8_t>((w[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-            h[i] = __half_as_ushort(__short2half_rn(static_cast<short>(b)));
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            h[i] = i < valid ? __half_as_ushort(__short2half_rn(static_cast<short>(src[i]))) : 0;
-    }
-    // room: fp16 slots left in the destination row (a multiple of 8)
-    uint4 o0, o1;
-    o0.x = h[0] | (uint32_t(h[1]) << 16);
-    o0.y = h[2] | (uint32_t(h[3]) << 16);
-    o0.z = h[4] | (uint32_t(h[5]) << 16);
-    o0.w = h[6] | (uint32_t(h[7]) << 16);
-    o1.x = h[8] | (uint32_t(h[9]) << 16);
-    o1.y = h[10] | (uint32_t(h[11]) << 16);
-    o1.z = h[12] | (uint32_t(h[13]) << 16);
-    o1.w = h[14] | (uint32_t(h[15]) << 16);
-    reinterpret_cast<uint4 *>(dst)[0] = o0;
-    if (room > 8) reinterpret_cast<uint4 *>(dst)[1] = o1;
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
-// Rows [0, rowsA) of the flattened row range belong to A, the rest to B.
-// Each destination row has `pitch` (a multiple of 8) fp16 slots; the slots
-// past the source columns are written as zero.
-__global__ void widen_s8_f16_kernel(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16,
-                                    int64_t pitchA, const int8_t *B, int64_t rowsB, int64_t colsB,
-                                    uint16_t *B16, int64_t pitchB)
+struct WidenJob {
+    const int8_t *src;
+    int64_t rows, cols;
+    uint16_t *dst;
+    int64_t pitch;  // destination row pitch in elements, a multiple of 8
+};
+
+// One 16-element piece of one row: loads the source bytes (one 16-byte load
+// when the row is 16-byte aligned and the piece is whole, else byte loads),
+// writes 16 fp16 values (the slots past `cols` as zero).
+__device__ __forceinline__ void widen_piece(const WidenJob &j, int64_t r, int64_t c)
 {
-    const int64_t rows = rowsA + rowsB;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const bool isA = r < rowsA;
-        const int64_t row = isA ? r : r - rowsA;
-        const int64_t cols = isA ? colsA : colsB;
-        const int64_t pitch = isA ? pitchA : pitchB;
-        const int8_t *src = (isA ? A : B) + row * cols;
-        uint16_t *dst = (isA ? A16 : B16) + row * pitch;
-        for (int64_t c = 16 * static_cast<int64_t>(threadIdx.x); c < pitch; c += 16 * blockDim.x)
-            widen16(src + c, cols - c, dst + c, pitch - c);
+    const int8_t *src = j.src + r * j.cols + c;
+    const int64_t valid = j.cols - c;
+    uint32_t w[4];
+    if (valid >= 16 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (4 * q + b < valid) x |= static_cast<uint32_t>(static_cast<uint8_t>(src[4 * q + b])) << (8 * b);
+            w[q] = x;
+        }
     }
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) widen4(w[q], o[2 * q], o[2 * q + 1]);
+    if (valid < 16) {
+        // Bytes past the row were read as 0 and widen to 0 already; the mask
+        // keeps the zero padding independent of that.
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t e = 2 * q;
+            const uint32_t keep = (e < valid ? 0x0000FFFFu : 0u) | (e + 1 < valid ? 0xFFFF0000u : 0u);
+            o[q] &= keep;
+        }
+    }
+    uint16_t *dst = j.dst + r * j.pitch + c;
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (j.pitch - c > 8) reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// blockIdx.z picks the matrix (0: A, 1: B); x covers 16-element pieces of a
+// row, y strides over rows, two rows in flight per thread.
+__global__ void widen_s8_f16_kernel(const WidenJob ja, const WidenJob jb)
+{
+    const WidenJob &j = blockIdx.z == 0 ? ja : jb;
+    const int64_t c = 16 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+    if (c >= j.pitch) return;
+    const int64_t step = gridDim.y;
+    int64_t r = blockIdx.y;
+    for (; r + step < j.rows; r += 2 * step) {
+        widen_piece(j, r, c);
+        widen_piece(j, r + step, c);
+    }
+    if (r < j.rows) widen_piece(j, r, c);
+}
+
+// Copies a rows x cols fp16 matrix (densely packed, any 2-byte alignment)
+// into a destination whose row pitch `pitch` is a multiple of 8 elements,
+// the slots past `cols` set to zero.  Each thread writes 8 elements (16
+// bytes) of a row: it reads the two naturally aligned 16-byte words that
+// hold them -- each is read only if it contains a byte of the row, so no
+// read leaves the source allocation -- and shifts them into place.
+struct PadJob {
+    const uint16_t *src;
+    int64_t rows, cols;
+    uint16_t *dst;
+    int64_t pitch;
+};
+
+__device__ __forceinline__ void pad_piece(const PadJob &j, int64_t r, int64_t c)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(j.src + r * j.cols);
+    const uintptr_t hi = lo + 2 * static_cast<uintptr_t>(j.cols);
+    const uintptr_t a = lo + 2 * static_cast<uintptr_t>(c);
+    const uint32_t s = static_cast<uint32_t>(a & 15u);
+    const uintptr_t base = a - s;
+    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
+    if (base < hi && base + 16 > lo) w0 = __ldg(reinterpret_cast<const uint4 *>(base));
+    if (s != 0 && base + 16 < hi) w1 = __ldg(reinterpret_cast<const uint4 *>(base + 16));
+    uint32_t o[4];
+    realign16(w0, w1, s, o);
+    const int64_t valid = j.cols - c;
+    if (valid < 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t keep = (2 * i < valid ? 0x0000FFFFu : 0u) | (2 * i + 1 < valid ? 0xFFFF0000u : 0u);
+            o[i] &= keep;
+        }
+    }
+    *reinterpret_cast<uint4 *>(j.dst + r * j.pitch + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// x covers 8-element pieces of a row, y strides over rows, two rows in
+// flight per thread.
+__global__ void pad_f16_kernel(const PadJob j)
+{
+    const int64_t c = 8 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+    if (c >= j.pitch) return;
+    const int64_t step = gridDim.y;
+    int64_t r = blockIdx.y;
+    for (; r + step < j.rows; r += 2 * step) {
+        pad_piece(j, r, c);
+        pad_piece(j, r + step, c);
+    }
+    if (r < j.rows) pad_piece(j, r, c);
 }
 
 __global__ void zero_fill_kernel(uint8_t *dst, int64_t bytes)
@@ -95,13 +177,32 @@ cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, u
                                 const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB,
                                 int sms, cudaStream_t s)
 {
-    const int64_t rows = rowsA + rowsB;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    const int grid = static_cast<int>(rows < cap ? rows : cap);
+    const WidenJob ja{A, rowsA, colsA, A16, pitchA};
+    const WidenJob jb{B, rowsB, colsB, B16, pitchB};
+    const int threads = 128;
     const int64_t maxpitch = pitchA > pitchB ? pitchA : pitchB;
-    int threads = static_cast<int>((maxpitch + 15) / 16);
-    threads = threads < 32 ? 32 : (threads > 256 ? 256 : (threads + 31) / 32 * 32);
-    widen_s8_f16_kernel<<<grid, threads, 0, s>>>(A, rowsA, colsA, A16, pitchA, B, rowsB, colsB, B16, pitchB);
+    const int64_t gx = ((maxpitch + 15) / 16 + threads - 1) / threads;
+    const int64_t maxrows = rowsA > rowsB ? rowsA : rowsB;
+    // About eight blocks of 128 threads per SM for each matrix.
+    int64_t gy = (static_cast<int64_t>(sms) * 8 + gx - 1) / gx;
+    gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
+    gy = gy > 65535 ? 65535 : gy;
+    if (gx > 2147483647) return cudaErrorInvalidValue;
+    widen_s8_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2), threads, 0, s>>>(ja, jb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_f16(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch, int sms,
+                           cudaStream_t s)
+{
+    const PadJob j{src, rows, cols, dst, pitch};
+    const int threads = 128;
+    const int64_t gx = (pitch / 8 + threads - 1) / threads;
+    int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
+    gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
+    gy = gy > 65535 ? 65535 : gy;
+    if (gx > 2147483647) return cudaErrorInvalidValue;
+    pad_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1), threads, 0, s>>>(j);
     return cudaGetLastError();
 }
 

@@ -127,6 +127,26 @@ struct Waiter {
 
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
+// Work of one task: an output tile at (m0, n0) that is BN or BN/2 wide.
+// Tasks [0, full_tasks) are whole tiles in m-fastest order; the tiles after
+// them (the last, partial wave of a persistent grid) are split into two
+// half-width tasks each, so the last wave has more, shorter tasks.
+struct Task {
+    int64_t m0, n0;
+    int bn;
+};
+
+template <class Cfg>
+__device__ __forceinline__ Task task_of(const GemmParams &p, int64_t u)
+{
+    if (u < p.full_tasks) {
+        return Task{(u % p.m_tiles) * Cfg::BM, (u / p.m_tiles) * Cfg::BN, Cfg::BN};
+    }
+    const int64_t h = u - p.full_tasks;
+    const int64_t t = p.full_tasks + (h >> 1);
+    return Task{(t % p.m_tiles) * Cfg::BM, (t / p.m_tiles) * Cfg::BN + (h & 1) * (Cfg::BN / 2), Cfg::BN / 2};
+}
+
 // ------------------------------------------------------------ TMA producer
 
 template <class Cfg>
@@ -138,9 +158,12 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
     uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arm
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-        const int32_t m0 = static_cast<int32_t>((t % p.m_tiles) * Cfg::BM);
-        const int32_t n0 = static_cast<int32_t>((t / p.m_tiles) * Cfg::BN);
+    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+        const Task tk = task_of<Cfg>(p, u);
+        const int32_t m0 = static_cast<int32_t>(tk.m0);
+        const int32_t n0 = static_cast<int32_t>(tk.n0);
+        const int nb64 = tk.bn / 64;
+        const uint32_t stage_bytes = Cfg::A_BYTES + tk.bn * Cfg::BK * 2;
         for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
                 ok = false;
@@ -150,11 +173,11 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
                 const uint32_t fb = smem_u32(&ctl->full[stage]);
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
-                mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, stage_bytes);
                 tma_load_2d(sa, tA, fb, k0, m0);
 #pragma unroll
                 for (int j = 0; j < Cfg::NB64; ++j)
-                    tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                    if (j < nb64) tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -182,26 +205,6 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
 // containing at least one byte of the row (so never outside the allocation),
 // realigned across neighbouring lanes with shuffles and funnel shifts, and
 // masked to zero outside the matrix (rows >= M or K, columns >= K or N).
-
-__device__ __forceinline__ void realign16(const uint4 &lo, const uint4 &hi, uint32_t s, uint32_t (&o)[4])
-{
-    // o = bytes [s, s + 16) of the 32-byte window lo:hi (s even, 0..14)
-    const uint32_t q = s >> 2, sh = (s & 3u) * 8u;
-    uint32_t a0, a1, a2, a3, a4;
-    if (q == 0) {
-        a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x;
-    } else if (q == 1) {
-        a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y;
-    } else if (q == 2) {
-        a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z;
-    } else {
-        a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w;
-    }
-    o[0] = __funnelshift_r(a0, a1, sh);
-    o[1] = __funnelshift_r(a1, a2, sh);
-    o[2] = __funnelshift_r(a2, a3, sh);
-    o[3] = __funnelshift_r(a3, a4, sh);
-}
 
 struct SegLoad {
     uint4 lo, ex;
@@ -273,9 +276,11 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
     int stage = 0;
     uint32_t phase = 0;
     int64_t kb_count = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-        const int64_t m0 = (t % p.m_tiles) * Cfg::BM;
-        const int64_t n0 = (t / p.m_tiles) * Cfg::BN;
+    // The host gives this producer whole tiles only (full_tasks == tasks).
+    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+        const Task tk = task_of<Cfg>(p, u);
+        const int64_t m0 = tk.m0;
+        const int64_t n0 = tk.n0;
         for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
             const int64_t k0 = kb * Cfg::BK;
             const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
@@ -328,12 +333,14 @@ template <class Cfg>
 __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
                            Ctl<Cfg::STAGES> *ctl, const Waiter &w)
 {
-    constexpr uint32_t IDESC = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
+    constexpr uint32_t IDESC_FULL = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
+    constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(Cfg::BM, Cfg::BN / 2, true);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
-    for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+        const uint32_t idesc = task_of<Cfg>(p, u).bn == Cfg::BN ? IDESC_FULL : IDESC_HALF;
         for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
             const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
             if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
@@ -354,7 +361,7 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                 for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
                     const uint64_t da = umma_desc_sw128(sa + kk * 32, 16, 1024);
                     const uint64_t db = umma_desc_sw128(sb + kk * 2048, 8192, 1024);
-                    umma_f16(d, da, db, IDESC, (kb > kc || kk > 0) ? 1u : 0u);
+                    umma_f16(d, da, db, idesc, (kb > kc || kk > 0) ? 1u : 0u);
                 }
                 issued = true;
                 umma_commit(smem_u32(&ctl->empty[stage]));
@@ -429,9 +436,11 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
     const int h = e >> 2;                  // column half of the tile
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-        const int64_t row0 = (t % p.m_tiles) * Cfg::BM + q * 32;
-        const int64_t colb = (t / p.m_tiles) * Cfg::BN + h * Cfg::EPI_COLS;
+    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+        const Task tk = task_of<Cfg>(p, u);
+        const int ncols = tk.bn / 2;  // this warp's columns
+        const int64_t row0 = tk.m0 + q * 32;
+        const int64_t colb = tk.n0 + h * ncols;
         uint32_t isum[Cfg::INT_OUT ? Cfg::EPI_COLS : 1];
         if constexpr (Cfg::INT_OUT) {
 #pragma unroll
@@ -441,20 +450,31 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             const bool got = w.wait(smem_u32(&ctl->tfull[acc]), acc_phase);
             if (!__all_sync(0xffffffffu, got)) return;
             tc_fence_after_sync();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * Cfg::EPI_COLS;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * ncols;
+            if constexpr (Cfg::INT_OUT) {
+                // Chunk partials are integers below 2^24 in magnitude: exact
+                // in fp32, so the conversion is exact.  16 columns per load
+                // keep the 128 running sums in registers.
 #pragma unroll
-            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + jb * 32, r);
-                tmem_wait_ld();
-                if constexpr (Cfg::INT_OUT) {
-                    // Chunk partials are integers below 2^24 in magnitude:
-                    // exact in fp32, so the conversion is exact.
+                for (int jb = 0; jb < Cfg::EPI_COLS / 16; ++jb) {
+                    if (jb < ncols / 16) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tbase + jb * 16, r);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        isum[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-                } else {
-                    store_block(p, stg, r, row0, colb + jb * 32, lane);
+                        for (int i = 0; i < 16; ++i)
+                            isum[jb * 16 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
+                    if (jb < ncols / 32) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                        tmem_wait_ld();
+                        store_block(p, stg, r, row0, colb + jb * 32, lane);
+                    }
                 }
             }
             tc_fence_before_sync();
@@ -465,7 +485,8 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
         }
         if constexpr (Cfg::INT_OUT) {
 #pragma unroll
-            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
+            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb)
+                if (jb < ncols / 32) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
         }
     }
 }

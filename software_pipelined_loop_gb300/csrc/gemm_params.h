@@ -14,7 +14,9 @@ struct GemmParams {
     int64_t ldb;
     void *C;  // float or int32, M x N, row pitch ldc elements
     int64_t ldc;
-    int64_t m_tiles, tiles;
+    int64_t m_tiles, tiles;  // BM x BN tile grid (m fastest)
+    int64_t full_tasks;      // tasks that are whole tiles: [0, full_tasks)
+    int64_t tasks;           // whole tiles, then the tail tiles split into two BN/2 halves
     int64_t num_kb;        // ceil(K / BK)
     int64_t kb_per_chunk;  // k-blocks per TMEM accumulation unit
     int vec_store;         // C base and pitch allow 16-byte stores

@@ -119,7 +119,7 @@ StallHook g_stall;
 struct Plan {
     const Variant *v = nullptr;
     int grid = 0;
-    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0;
+    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0, full_tasks = 0, tasks = 0;
     int vec_store = 0;
 };
 
@@ -161,6 +161,15 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
     pl->grid = static_cast<int>(pl->tiles < d.sms ? pl->tiles : d.sms);
+    // Balance the last wave: if the tiles left after the full waves fit
+    // twice over into the grid, each is done as two half-width tasks.
+    const int64_t rem = pl->tiles % pl->grid;
+    pl->full_tasks = pl->tiles;
+    pl->tasks = pl->tiles;
+    if (v->info.producer == 0 && rem > 0 && 2 * rem <= pl->grid && pl->tiles > pl->grid) {
+        pl->full_tasks = pl->tiles - rem;
+        pl->tasks = pl->tiles + rem;
+    }
     pl->vec_store = aligned16(C) && (ldc * 4) % 16 == 0;
     return GEMMPIPE_OK;
 }
@@ -303,6 +312,8 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
     p.ldc = ldc;
     p.m_tiles = pl.m_tiles;
     p.tiles = pl.tiles;
+    p.full_tasks = pl.full_tasks;
+    p.tasks = pl.tasks;
     p.num_kb = pl.num_kb;
     p.kb_per_chunk = pl.kb_per_chunk;
     p.vec_store = pl.vec_store;
@@ -341,6 +352,29 @@ gemmpipe_status_t zero_c(void *C, int64_t bytes, const DeviceInfo &d, cudaStream
 
 int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
 
+// TMA can describe a row-major fp16 operand whose base and row pitch are
+// multiples of 16 bytes.
+bool operand_tma_ok(const void *p, int64_t ld) { return aligned16(p) && (ld * 2) % 16 == 0; }
+
+// Misaligned fp16 operands are padded unless the bounded-load producer is forced.
+bool pad_wanted(const void *A, int64_t K, const void *B, int64_t N)
+{
+    if (operand_tma_ok(A, K) && operand_tma_ok(B, N)) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_override.producer != 1;
+}
+
+gemmpipe_status_t pad_operand(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch,
+                              const DeviceInfo &d, cudaStream_t s)
+{
+    TimedRegion tr(false, s);
+    const cudaError_t e = gp::launch_pad_f16(src, rows, cols, dst, pitch, d.sms, s);
+    tr.end();
+    if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    return GEMMPIPE_OK;
+}
+
 int64_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return 2 * (M * round8(K) + K * round8(N)); }
 
 }  // namespace
@@ -353,13 +387,39 @@ gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_ha
     gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 2, 4);
     if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
     DeviceInfo d;
-    if ((st = device_info(&d, nullptr)) != GEMMPIPE_OK) return st;
+    int dev = 0;
+    if ((st = device_info(&d, &dev)) != GEMMPIPE_OK) return st;
     if ((st = check_device_pointers(K, A, B, C, 2, 4)) != GEMMPIPE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, M * N * 4, d, s);
+    const uint16_t *Ause = A, *Buse = B;
+    int64_t lda = K, ldb = N;
+    if (pad_wanted(A, K, B, N)) {
+        // "Pad the matrices" remedy: aligned copies in the stream's workspace,
+        // then the TMA producer.  Without a workspace the bounded-load
+        // producer reads the original operands instead.
+        const bool pa = !operand_tma_ok(A, K), pb = !operand_tma_ok(B, N);
+        const int64_t Kp = round8(K), Np = round8(N);
+        const int64_t bytes = (pa ? 2 * M * Kp : 0) + (pb ? 2 * K * Np : 0);
+        void *ws = nullptr;
+        if (workspace(dev, s, bytes, &ws) == GEMMPIPE_OK) {
+            uint16_t *w = static_cast<uint16_t *>(ws);
+            if (pa) {
+                if ((st = pad_operand(A, M, K, w, Kp, d, s)) != GEMMPIPE_OK) return st;
+                Ause = w;
+                lda = Kp;
+                w += M * Kp;
+            }
+            if (pb) {
+                if ((st = pad_operand(B, K, N, w, Np, d, s)) != GEMMPIPE_OK) return st;
+                Buse = w;
+                ldb = Np;
+            }
+        }
+    }
     Plan pl;
-    if ((st = make_plan(false, M, N, K, A, K, B, N, C, N, d, &pl)) != GEMMPIPE_OK) return st;
-    return run_plan(pl, false, M, N, K, A, K, B, N, C, N, s);
+    if ((st = make_plan(false, M, N, K, Ause, lda, Buse, ldb, C, N, d, &pl)) != GEMMPIPE_OK) return st;
+    return run_plan(pl, false, M, N, K, Ause, lda, Buse, ldb, C, N, s);
 }
 
 gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B, int32_t *C,
@@ -450,6 +510,10 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
 {
     if (!plan || (dtype != 0 && dtype != 1)) return GEMMPIPE_ERR_INVALID_VALUE;
     const bool s8 = dtype == 0;
+    static const uint16_t *const kAligned = reinterpret_cast<const uint16_t *>(256);
+    if (!A) A = kAligned;
+    if (!B) B = kAligned;
+    if (!C) C = kAligned;
     gemmpipe_status_t st = check_shape(M, N, K, A, B, C, s8 ? 1 : 2, 4);
     if (st != GEMMPIPE_OK) return st;
     DeviceInfo d;
@@ -459,8 +523,13 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     Plan pl;
     if (s8) {
         // The widened copies are 16-byte aligned with 16-byte row pitches.
-        static const uint16_t *const kAligned = reinterpret_cast<const uint16_t *>(256);
         st = make_plan(true, M, N, K, kAligned, round8(K), kAligned, round8(N), C, N, d, &pl);
+    } else if (pad_wanted(A, K, B, N)) {
+        const bool pa = !operand_tma_ok(A, K), pb = !operand_tma_ok(B, N);
+        st = make_plan(false, M, N, K, pa ? kAligned : A, pa ? round8(K) : K, pb ? kAligned : B,
+                       pb ? round8(N) : N, C, N, d, &pl);
+        plan->workspace_bytes = (pa ? 2 * M * round8(K) : 0) + (pb ? 2 * K * round8(N) : 0);
+        plan->operand_copy = 2;
     } else {
         st = make_plan(false, M, N, K, A, K, B, N, C, N, d, &pl);
     }
@@ -475,10 +544,14 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     plan->threads = f.threads;
     plan->grid = pl.grid;
     plan->tiles = pl.tiles;
+    plan->tasks = pl.tasks;
     plan->k_blocks = pl.num_kb;
     plan->smem_bytes = f.smem_bytes;
     plan->vector_store = pl.vec_store;
-    plan->workspace_bytes = s8 ? s8_workspace_bytes(M, N, K) : 0;
+    if (s8) {
+        plan->workspace_bytes = s8_workspace_bytes(M, N, K);
+        plan->operand_copy = 1;
+    }
     return GEMMPIPE_OK;
 }
 

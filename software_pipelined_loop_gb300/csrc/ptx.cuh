@@ -181,6 +181,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -260,6 +272,28 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// o = bytes [s, s + 16) of the 32-byte window lo:hi (s even, 0..14): the
+// realignment step of every misaligned 16-byte fetch in this library.
+__device__ __forceinline__ void realign16(const uint4 &lo, const uint4 &hi, uint32_t s, uint32_t (&o)[4])
+{
+    // o = bytes [s, s + 16) of the 32-byte window lo:hi (s even, 0..14)
+    const uint32_t q = s >> 2, sh = (s & 3u) * 8u;
+    uint32_t a0, a1, a2, a3, a4;
+    if (q == 0) {
+        a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x;
+    } else if (q == 1) {
+        a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y;
+    } else if (q == 2) {
+        a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z;
+    } else {
+        a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w;
+    }
+    o[0] = __funnelshift_r(a0, a1, sh);
+    o[1] = __funnelshift_r(a1, a2, sh);
+    o[2] = __funnelshift_r(a2, a3, sh);
+    o[3] = __funnelshift_r(a3, a4, sh);
 }
 
 }  // namespace gp

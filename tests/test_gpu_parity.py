@@ -138,13 +138,20 @@ def test_misaligned_base_pointers(dev):
     ab[1:1 + M * K] = to_dev(A.reshape(-1), dev)
     bb[1:1 + K * N] = to_dev(B.reshape(-1), dev)
     a_ptr, b_ptr, c_ptr = ab.data_ptr() + 2, bb.data_ptr() + 2, cb.data_ptr() + 4
-    plan = gemmpipe.gemmpipe_plan(1, M, N, K, a_ptr, b_ptr, c_ptr)
-    assert plan["producer"] == 1 and plan["vector_store"] == 0
-    gemmpipe.gemm_f16f32(M, N, K, a_ptr, b_ptr, c_ptr)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
-    got = cb[1:1 + M * N].cpu().numpy().reshape(M, N)
-    assert_f16_close(got, oracle.gemm_f16f32(A, B))
-    assert cb[0].item() == 0 and cb[M * N + 1:].abs().sum().item() == 0
+    ref = oracle.gemm_f16f32(A, B)
+    for forced, producer, copy in ((-1, 0, 2), (1, 1, 0)):
+        gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
+        try:
+            plan = gemmpipe.gemmpipe_plan(1, M, N, K, a_ptr, b_ptr, c_ptr)
+            assert plan["producer"] == producer and plan["operand_copy"] == copy and plan["vector_store"] == 0
+            cb.zero_()
+            gemmpipe.gemm_f16f32(M, N, K, a_ptr, b_ptr, c_ptr)
+            assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+        finally:
+            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+        got = cb[1:1 + M * N].cpu().numpy().reshape(M, N)
+        assert_f16_close(got, ref)
+        assert cb[0].item() == 0 and cb[M * N + 1:].abs().sum().item() == 0
 
 
 def test_guard_bands_untouched(dev):
@@ -236,14 +243,20 @@ def test_workload_fp16_skinny_sampled(dev):
     assert np.isfinite(got).all()
 
 
-def test_workload_fp16_ragged_sampled(dev):
+@pytest.mark.parametrize("forced", [-1, 1], ids=["padded_tma", "bounded_loads"])
+def test_workload_fp16_ragged_sampled(dev, forced):
     _, _, M, N, K, A, B = inputs.workload_operands(4)
-    plan = gemmpipe.gemmpipe_plan(1, M, N, K)
-    got = run_f16(A, B, dev)
     rows = sample_rows(M)
-    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "ragged")
-    assert np.isfinite(got).all()
+    ref = oracle.gemm_f16f32(A, B, rows=rows)
+    gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert plan["k_blocks"] == (K + 63) // 64
+    assert_f16_close(got[rows], ref, "ragged")
+    assert np.isfinite(got).all()
 
 
 # --------------------------------------------------------- bounded waits
@@ -265,15 +278,20 @@ def test_stall_times_out_and_context_survives(dev):
 
 def test_stall_times_out_bounded_load_producer(dev):
     import torch
-    M, N, K = 129, 200, 333   # odd pitches: bounded-load producer
+    M, N, K = 129, 200, 333   # odd pitches; the bounded-load producer is forced
     A, B = inputs.make_operands("f16", M, N, K, seed=14)
     Ad, Bd = to_dev(A, dev), to_dev(B, dev)
     C = torch.zeros((M, N), dtype=torch.float32, device=dev)
-    gemmpipe.gemmpipe_test_inject_stall(1, 200)
-    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
-    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    gemmpipe.gemmpipe_set_plan_override(1, 0, 0)
+    try:
+        assert gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)["producer"] == 1
+        gemmpipe.gemmpipe_test_inject_stall(1, 200)
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
@@ -307,3 +325,44 @@ def test_copy_kernel(dev):
     gemmpipe.gemmpipe_copy(odd.data_ptr() + 1, src.data_ptr() + 3, 999)
     assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
     assert torch.equal(odd[1:1000].cpu(), src.cpu().view(torch.uint8)[3:1002])
+
+
+# ---------------------------------------------------- last-wave task split
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("wide", [True, False], ids=["bn256", "bn128"])
+def test_tail_wave_split(dev, dtype, wide):
+    # Tile counts a little above one wave of the persistent grid: the tiles of
+    # the last, partial wave run as two half-width tasks each.
+    G = gemmpipe.gemmpipe_plan(1, 4096, 4096, 4096)["grid"]
+    target = G + max(1, G // 4)
+    if wide:
+        n_tiles, N = 2, 504
+        K = 136
+    else:
+        n_tiles, N = 1, 120
+        K = 200
+    m_tiles = -(-target // n_tiles)
+    M = m_tiles * 128 - 5
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    tiles = m_tiles * n_tiles
+    rem = tiles % G
+    assert plan["tiles"] == tiles and plan["BN"] == (256 if wide else 128)
+    assert 0 < rem and 2 * rem <= G and plan["tasks"] == tiles + rem
+    A, B = inputs.make_operands(dtype, M, N, K, seed=500 + M)
+    if dtype == "s8":
+        assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+def test_workload_fp16_4096_sampled(dev):
+    # The fp16 half of the headline metric: 4096^3, uniform [-1, 1]; 512
+    # tiles leave a last wave that runs as half-width tasks.
+    M = N = K = 4096
+    A, B = inputs.make_operands("f16", M, N, K, seed=inputs.SEED_BASE + 5)
+    plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+    assert plan["tasks"] >= plan["tiles"]
+    got = run_f16(A, B, dev)
+    rows = sample_rows(M)
+    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "fp16 4096^3")
