@@ -45,7 +45,8 @@
  * guarded by a mutex.
  *
  * Error behaviour common to the GEMM entry points:
- *   - M, N or K negative, any of them above 2^31 - 1, a null A/B with
+ *   - M, N or K negative, any of them above 2^31 - 1, a matrix of 2^56
+ *     elements or more, a null A/B with
  *     M*N*K > 0, a null C with M*N > 0, a pointer not aligned to its element
  *     size, or a pointer the CUDA runtime does not know as device or managed
  *     memory                                   -> GEMMPIPE_ERR_INVALID_VALUE

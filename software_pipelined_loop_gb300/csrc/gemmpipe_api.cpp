@@ -82,6 +82,12 @@ gemmpipe_status_t check_shape(int64_t M, int64_t N, int64_t K, const void *A, co
                               int ab_bytes, int c_bytes)
 {
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMMPIPE_ERR_INVALID_VALUE;
+    // No matrix (or padded copy of one) may hold 2^56 elements or more, so
+    // that byte counts of operands and workspaces stay far inside int64.
+    constexpr int64_t kMaxElems = int64_t(1) << 56;
+    if ((K > 0 && M > kMaxElems / (K + 8)) || (N > 0 && K > kMaxElems / (N + 8)) ||
+        (N > 0 && M > kMaxElems / N))
+        return GEMMPIPE_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMMPIPE_OK;
     if (!C) return GEMMPIPE_ERR_INVALID_VALUE;
     if (K > 0 && (!A || !B)) return GEMMPIPE_ERR_INVALID_VALUE;

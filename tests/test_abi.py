@@ -60,6 +60,9 @@ def test_host_side_argument_checks(lib):
     assert f16(-1, 4, 4, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
     assert s8(4, 4, -2, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
     assert f16(1 << 31, 4, 4, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
+    big = (1 << 31) - 1
+    assert s8(big, 8, big, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE    # 2^62 elements of A
+    assert f16(big, big, 8, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE   # 2^62 elements of C
     assert f16(4, 4, 4, None, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
     assert s8(4, 4, 4, fake, fake, None, None) == gemmpipe.ERR_INVALID_VALUE
     assert f16(4, 4, 4, fake + 1, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE   # fp16 misaligned
