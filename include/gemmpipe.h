@@ -124,6 +124,44 @@ GEMMPIPE_API gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K,
                               float *C, gemmpipe_stream_t stream);
 
 /*
+ * gemm_s8s8s32 for callers that cannot let a library allocate GPU memory.
+ * The pages have no counterpart of this entry point.
+ *
+ * Who needs it: a process that has planned every byte of device memory up
+ * front (for example a server whose own pool owns all free memory, or code
+ * with a certified static memory budget), and code on a latency-critical
+ * path where a cudaMalloc or cudaFree inside the call would stall the whole
+ * device.  gemm_s8s8s32 itself may cudaMalloc (and cudaFree) its workspace;
+ * this entry point never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ * How: the fp16 copies of A and B live in one fixed scratch array of
+ * GEMMPIPE_NOALLOC_SCRATCH_BYTES that the library declares statically in
+ * device memory.  Every GPU on which the library is loaded holds that array
+ * until the process exits.  The caller still passes A, B and C.
+ *
+ * Limits and behaviour:
+ *   - needs 2 * (M * Kp + K * Np) <= GEMMPIPE_NOALLOC_SCRATCH_BYTES, with
+ *     Kp and Np = K and N rounded up to a multiple of 8 (e.g. M = N = K =
+ *     2048 fits, 4096^3 does not); larger problems return
+ *     GEMMPIPE_ERR_INVALID_VALUE before anything is launched;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current, and keeps it; make
+ *     that first call before any stream capture;
+ *   - all calls share the one array and it keeps whatever the last call
+ *     left there; nothing in it has to start at zero, because each call
+ *     writes every scratch element it later reads;
+ *   - calls whose work overlaps on the GPU (different streams, or several
+ *     host threads without ordering) race on the array and give wrong
+ *     results: order them, e.g. on one stream;
+ *   - otherwise the same arguments, result and errors as gemm_s8s8s32.
+ */
+#define GEMMPIPE_NOALLOC_SCRATCH_BYTES (16u << 20)
+GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32_noalloc(int64_t M, int64_t N, int64_t K,
+                                                    const int8_t *A, const int8_t *B, int32_t *C,
+                                                    gemmpipe_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the current device's error
  * word.  Returns GEMMPIPE_ERR_TIMEOUT if a kernel of this library gave up on
  * a pipeline wait (every wait is bounded; the kernel then stops issuing

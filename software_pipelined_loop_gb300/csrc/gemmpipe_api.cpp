@@ -385,6 +385,75 @@ int64_t s8_workspace_bytes(int64_t M, int64_t N, int64_t K) { return 2 * (M * ro
 
 }  // namespace
 
+namespace gp {
+
+// The INT8 flow of gemm_s8s8s32 with caller-provided scratch for the fp16
+// copies: no workspace allocation and no timing events.  Used only by
+// gemm_s8s8s32_noalloc.
+gemmpipe_status_t s8_check_fixed_scratch(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B,
+                                         const int32_t *C, int64_t scratch_bytes)
+{
+    const gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 1, 4);
+    if (st != GEMMPIPE_OK) return st;
+    if (M == 0 || N == 0 || K == 0) return GEMMPIPE_OK;
+    return s8_workspace_bytes(M, N, K) <= scratch_bytes ? GEMMPIPE_OK : GEMMPIPE_ERR_INVALID_VALUE;
+}
+
+gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B,
+                                        int32_t *C, cudaStream_t s, uint16_t *scratch, int64_t scratch_bytes)
+{
+    gemmpipe_status_t st = s8_check_fixed_scratch(M, N, K, A, B, C, scratch_bytes);
+    if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
+    DeviceInfo d;
+    if ((st = device_info(&d, nullptr)) != GEMMPIPE_OK) return st;
+    if ((st = check_device_pointers(K, A, B, C, 1, 4)) != GEMMPIPE_OK) return st;
+    if (K == 0) {
+        if (gp::launch_zero_fill(C, M * N * 4, d.sms, s) != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+        g_launches.fetch_add(1);
+        return GEMMPIPE_OK;
+    }
+    const int64_t Kp = round8(K), Np = round8(N);
+    uint16_t *A16 = scratch;
+    uint16_t *B16 = scratch + M * Kp;
+    if (gp::launch_widen_s8_f16(A, M, K, A16, Kp, B, K, N, B16, Np, d.sms, s) != cudaSuccess)
+        return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    Plan pl;
+    if ((st = make_plan(true, M, N, K, A16, Kp, B16, Np, C, N, d, &pl)) != GEMMPIPE_OK) return st;
+    CUtensorMap ta, tb;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (!encode_2d(&ta, A16, M, K, Kp, kBM) || !encode_2d(&tb, B16, K, N, Np, kBK)) return GEMMPIPE_ERR_INTERNAL;
+    GemmParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.A = A16;
+    p.lda = Kp;
+    p.B = B16;
+    p.ldb = Np;
+    p.C = C;
+    p.ldc = N;
+    p.m_tiles = pl.m_tiles;
+    p.tiles = pl.tiles;
+    p.full_tasks = pl.full_tasks;
+    p.tasks = pl.tasks;
+    p.num_kb = pl.num_kb;
+    p.kb_per_chunk = pl.kb_per_chunk;
+    p.vec_store = pl.vec_store;
+    p.stall_kb = -1;
+    p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
+    if (gp::status_word(&p.status) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    if (pl.v->launch(ta, tb, p, pl.grid, s) != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    g_launches.fetch_add(1);
+    return GEMMPIPE_OK;
+}
+
+}  // namespace gp
+
 extern "C" {
 
 gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_half_t *A, const gemmpipe_half_t *B,

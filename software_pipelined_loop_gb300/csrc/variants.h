@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "gemm_params.h"
+#include "gemmpipe.h"
 
 namespace gp {
 
@@ -37,5 +38,12 @@ cudaError_t launch_pad_f16(const uint16_t *src, int64_t rows, int64_t cols, uint
 cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t status_word(int **ptr);  // device address of the current device's status word
+
+// The INT8 flow with fixed, caller-provided scratch (gemmpipe_api.cpp), for
+// the no-allocation entry point.
+gemmpipe_status_t s8_check_fixed_scratch(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B,
+                                         const int32_t *C, int64_t scratch_bytes);
+gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B,
+                                        int32_t *C, cudaStream_t s, uint16_t *scratch, int64_t scratch_bytes);
 
 }  // namespace gp

@@ -20,6 +20,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "gemmpipe.h")
 STATUS = {0: "GEMMPIPE_OK", 1: "GEMMPIPE_ERR_INVALID_VALUE", 2: "GEMMPIPE_ERR_UNSUPPORTED_DEVICE",
           3: "GEMMPIPE_ERR_LAUNCH", 4: "GEMMPIPE_ERR_TIMEOUT", 5: "GEMMPIPE_ERR_INTERNAL",
           6: "GEMMPIPE_ERR_OUT_OF_MEMORY"}
+NOALLOC_SCRATCH_BYTES = 16 << 20  # GEMMPIPE_NOALLOC_SCRATCH_BYTES
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_INTERNAL, ERR_OUT_OF_MEMORY = range(7)
 
 
@@ -53,6 +54,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "gemm_s8s8s32": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemm_f16f32": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+        "gemm_s8s8s32_noalloc": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemmpipe_get_device_status": (_int, [_vp]),
         "gemmpipe_status_string": (ctypes.c_char_p, [_int]),
         "gemmpipe_compute_load_ratio": (ctypes.c_double, [_int, _int, _int, _int]),
@@ -113,6 +115,14 @@ def gemm_s8s8s32(M, N, K, A, B, C, stream=None) -> None:
 def gemm_f16f32(M, N, K, A, B, C, stream=None) -> None:
     """C (M x N fp32) = A (M x K fp16) @ B (K x N fp16), enqueued on `stream`."""
     _check(load().gemm_f16f32(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_f16f32")
+
+
+def gemm_s8s8s32_noalloc(M, N, K, A, B, C, stream=None) -> None:
+    """gemm_s8s8s32 that never allocates: the fp16 operand copies use the
+    library's fixed device scratch (NOALLOC_SCRATCH_BYTES), so problems
+    needing more are refused; calls overlapping on the GPU race on it."""
+    _check(load().gemm_s8s8s32_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)),
+           "gemm_s8s8s32_noalloc")
 
 
 def gemmpipe_get_device_status(stream=None) -> int:
