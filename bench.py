@@ -104,8 +104,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
+SHAPE = None  # (dtype, M, N, K) from --shape
+
+
 def workload(index: int):
     from software_pipelined_loop_gb300 import inputs
+    if index == HEADLINE and SHAPE is not None:
+        dt, M, N, K = SHAPE
+        A, B = inputs.make_operands(dt, M, N, K, inputs.SEED_BASE + 7)
+        return (f"{dt}_{M}x{N}x{K}", dt, M, N, K, A, B)
     return inputs.workload_operands(index)
 
 
@@ -321,6 +328,7 @@ def run_gpu(args) -> int:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * head["flops"] / ms / 1e9
+    unit = "TOPS" if head["dtype"] == "s8" else "TFLOPS"
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -329,7 +337,7 @@ def run_gpu(args) -> int:
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         r = cpu_oracle_rate(head["A"], head["B"], head["dtype"], target_s=args.cpu_seconds)
-        cpu = {"value": r["value"], "unit": "TOPS", "cores": r["cores"], "kind": "oracle",
+        cpu = {"value": r["value"], "unit": unit, "cores": r["cores"], "kind": "oracle",
                "sample": f"first {r['rows']} of {head['M']} rows of C (all {head['N']} columns, full K), "
                          f"{r['seconds']:.1f} s"}
 
@@ -342,14 +350,17 @@ def run_gpu(args) -> int:
                 "shape": [r["M"], r["N"], r["K"]]}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "s8",
-        "dtype_note": "int8 operands widened to fp16 (exact), tcgen05 kind::f16 with fp32 accumulation "
-                      "in <=1024-k chunks, exact int32 sum",
+        "vs_baseline": None, "dtype": head["dtype"],
+        "dtype_note": ("int8 operands widened to fp16 (exact), tcgen05 kind::f16 with fp32 accumulation "
+                       "in <=1024-k chunks, exact int32 sum") if head["dtype"] == "s8" else
+                      "fp16 operands, tcgen05 kind::f16, fp32 accumulation and output",
         "data": "synthetic",
         "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
-                   "l2": "256 MiB buffer written between timed steps (inputs 32 MiB < L2)",
+                   "l2": head["l2"] + " (256 MiB buffer written between timed steps when inputs < L2)",
+                   "plan": {k: head["plan"][k] for k in ("producer", "BN", "stages", "threads", "grid", "tasks",
+                                                         "operand_copy")},
                    "replicas": world},
         "roofline": head["roofline"],
         "cpu_baseline": cpu,
@@ -382,9 +393,24 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--shape", default=None,
+                    help="time dtype,M,N,K (s8 or f16) as the headline instead of INT8 4096^3 "
+                         "(for profiling and sweeps; uniform inputs)")
+    ap.add_argument("--force", default=None,
+                    help="plan override producer,bn,stages (see gemmpipe_set_plan_override)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.shape:
+        global SHAPE
+        dt, M, N, K = args.shape.split(",")
+        if dt not in ("s8", "f16"):
+            ap.error("--shape dtype must be s8 or f16")
+        SHAPE = (dt, int(M), int(N), int(K))
+    if args.force:
+        from software_pipelined_loop_gb300 import build, gemmpipe
+        build.build()
+        gemmpipe.gemmpipe_set_plan_override(*[int(x) for x in args.force.split(",")])
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

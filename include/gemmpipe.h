@@ -98,12 +98,16 @@ typedef enum {
  * operands that needs K > 131071).
  *
  * sm_103a has no integer tcgen05 MMA, so the operands are widened to fp16
- * (every int8 value is exact in fp16) into the library workspace, 2*(M*Kp +
- * K*Np) bytes with Kp, Np = K, N rounded up to a multiple of 8, and
- * multiplied on the fp16 tensor-core path with fp32 accumulation in chunks of
- * at most 1024 k values.  Each chunk's partial sums are integers of magnitude
- * <= 2^24, exact in fp32; the epilogue converts them to int32 and adds them.
- * Calls on one stream share that stream's workspace and are ordered by it.
+ * (every int8 value is exact in fp16) and multiplied on the fp16 tensor-core
+ * path with fp32 accumulation in chunks of at most 1024 k values.  Each
+ * chunk's partial sums are integers of magnitude <= 2^24, exact in fp32;
+ * they are converted to int32 and added.  The operands are first widened
+ * into the library workspace, 2*(M*Kp + K*Np) bytes with Kp, Np = K, N
+ * rounded up to a multiple of 8; calls on one stream share that stream's
+ * workspace and are ordered by it.  With the plan override producer = 0 and
+ * A, B on 16-byte boundaries with K and N multiples of 16, the kernel
+ * instead loads int8 tiles and widens them in shared memory (nothing is
+ * allocated; C also holds the running int32 sums between chunks).
  */
 GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K,
                                const int8_t *A, const int8_t *B, int32_t *C,
@@ -203,7 +207,8 @@ typedef struct {
     int64_t k_blocks;    /* ceil(K / BK) */
     int64_t smem_bytes;  /* dynamic shared memory per CTA */
     int vector_store;    /* 1: 16-byte stores of C, 0: 4-byte stores */
-    int operand_copy;    /* 0: none, 1: int8 widened to fp16, 2: misaligned fp16 padded */
+    int operand_copy;    /* 0: none (INT8: widened in the kernel), 1: int8 widened to fp16 in the
+                            workspace, 2: misaligned fp16 padded in the workspace */
     int64_t workspace_bytes; /* library workspace the call needs */
 } gemmpipe_plan_t;
 
@@ -222,7 +227,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
 /*
  * Overrides the plan for the following calls of this process (tests and the
  * stage/producer ablation).  producer: -1 automatic, 0 TMA (only honoured
- * where TMA can describe the operands), 1 bounded-load producer.  bn: 0
+ * where TMA can describe the operands; for gemm_s8s8s32 it selects the
+ * in-kernel widening of int8 tiles), 1 bounded-load producer for
+ * gemm_f16f32 and the workspace-widening path for gemm_s8s8s32.  bn: 0
  * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
  * depths (see gemmpipe_plan for what was taken).  Returns INVALID_VALUE for
  * values outside these sets.

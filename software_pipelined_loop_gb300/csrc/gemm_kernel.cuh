@@ -44,7 +44,7 @@ namespace gp {
 
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
-template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_>
+template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1>
 struct GemmCfg {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -58,32 +58,47 @@ struct GemmCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NB64 = BN / 64;  // 64-column B atoms per stage
 
+    // CONVERT: int8 operands arrive by TMA in an int8 ring; converter warps
+    // widen them to fp16 into the MMA's stage (INT8 path without a widening
+    // pass); chunk partials are accumulated in C itself.
+    static constexpr bool CONVERT = CONVERT_;
+    static constexpr int I8_STAGES = CONVERT ? I8_STAGES_ : 0;
+    static constexpr int I8_A_BYTES = BM * BK;
+    static constexpr int I8_B_BYTES = BK * BN;
+    static constexpr int I8_STAGE_BYTES = I8_A_BYTES + I8_B_BYTES;
+
     static constexpr int PRODUCER_WARPS = LDG ? 8 : 1;
     static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-    static constexpr int MMA_WARP = PRODUCER_WARPS;
+    static constexpr int CONV_WARPS = CONVERT ? 4 : 0;
+    static constexpr int CONV_THREADS = 32 * CONV_WARPS;
+    static constexpr int MMA_WARP = PRODUCER_WARPS + CONV_WARPS;
     static constexpr int EPI_WARP0 = MMA_WARP + 1;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = 32 * (PRODUCER_WARPS + 1 + EPI_WARPS);
+    static constexpr int THREADS = 32 * (PRODUCER_WARPS + CONV_WARPS + 1 + EPI_WARPS);
     static constexpr int EPI_COLS = BN / 2;  // columns per epilogue warp
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 
-    static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
+    static constexpr int I8_OFF = STAGES * STAGE_BYTES;
+    static constexpr int STAGING_OFF = I8_OFF + I8_STAGES * I8_STAGE_BYTES;
     static constexpr int STAGING_BYTES = EPI_WARPS * 32 * 128;
     static constexpr int CTL_OFF = STAGING_OFF + STAGING_BYTES;
-    static constexpr int CTL_BYTES = 8 * (2 * STAGES + 5) + 16;
+    static constexpr int CTL_BYTES = 8 * (2 * STAGES + 2 * I8_STAGES + 5) + 16;
     static constexpr int SMEM_BYTES = 1024 + CTL_OFF + CTL_BYTES;  // + alignment slack
 
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
+    static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
 };
 
-template <int STAGES>
+template <int STAGES, int I8_STAGES = 0>
 struct Ctl {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
+    uint64_t full_i8[I8_STAGES > 0 ? I8_STAGES : 1];
+    uint64_t empty_i8[I8_STAGES > 0 ? I8_STAGES : 1];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -150,8 +165,151 @@ __device__ __forceinline__ Task task_of(const GemmParams &p, int64_t u)
 // ------------------------------------------------------------ TMA producer
 
 template <class Cfg>
+__device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
+                                uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
+{
+    // int8 tiles: A box 64 (k) x 128 (rows), B box BN (n) x 64 (k), no
+    // swizzle; always the whole box (half-width tasks convert half of B).
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_par = 0;
+    int64_t kb_count = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+        const Task tk = task_of<Cfg>(p, u);
+        const int32_t m0 = static_cast<int32_t>(tk.m0);
+        const int32_t n0 = static_cast<int32_t>(tk.n0);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+            if (!w.wait(smem_u32(&ctl->empty_i8[stage]), phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) {
+                const uint32_t fb = smem_u32(&ctl->full_i8[stage]);
+                const uint32_t sa = sbase + Cfg::I8_OFF + stage * Cfg::I8_STAGE_BYTES;
+                const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
+                mbar_arrive_expect_tx(fb, Cfg::I8_STAGE_BYTES);
+                tma_load_2d(sa, tA, fb, k0, m0);
+                tma_load_2d(sa + Cfg::I8_A_BYTES, tB, fb, n0, k0);
+                armed |= 1u << stage;
+                armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
+            }
+            if (++stage == Cfg::I8_STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        for (int s = 0; s < Cfg::I8_STAGES; ++s)
+            if (armed & (1u << s))
+                w.wait_drain(smem_u32(&ctl->full_i8[s]), (armed_par >> s) & 1u, kDrainNs);
+    }
+}
+
+// ------------------------------------------------------ int8 -> fp16 converters
+//
+// Four warps widen each int8 k-block into the fp16 stage the MMA reads.  A
+// thread takes 16 int8 of one row (one 16-byte shared load), widens them
+// (bias by 128, place under the fp16 exponent of 1024, subtract 1152: exact
+// for every int8) and writes two 16-byte chunks in the 128-byte-swizzled
+// layout.  The int8 rows are 64 (A) or BN (B) bytes long, so a warp's loads
+// cover contiguous bytes; its stores hit each 16-byte bank group four times
+// per 512 bytes, the minimum.
+
+__device__ __forceinline__ void widen4_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+__device__ __forceinline__ void widen16_store(const uint4 &v, uint32_t dst_lo, uint32_t dst_hi)
+{
+    uint32_t o[8];
+    widen4_f16(v.x, o[0], o[1]);
+    widen4_f16(v.y, o[2], o[3]);
+    widen4_f16(v.z, o[4], o[5]);
+    widen4_f16(v.w, o[6], o[7]);
+    st_shared_v4(dst_lo, o[0], o[1], o[2], o[3]);
+    st_shared_v4(dst_hi, o[4], o[5], o[6], o[7]);
+}
+
+template <class Cfg>
+__device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
+                          const Waiter &w)
+{
+    const int ct = threadIdx.x - 32 * Cfg::PRODUCER_WARPS;  // 0 .. CONV_THREADS-1
+    constexpr int A_PIECES = Cfg::BM * (Cfg::BK / 16);       // 16 int8 per piece
+    constexpr int B_ROW_PIECES = Cfg::BN / 16;
+    constexpr int B_PIECES = Cfg::BK * B_ROW_PIECES;
+    static_assert(A_PIECES % Cfg::CONV_THREADS == 0 && B_PIECES % Cfg::CONV_THREADS == 0, "even split");
+    int si = 0, sf = 0;
+    uint32_t phi = 0, phf = 0;
+    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+        const int bn = task_of<Cfg>(p, u).bn;
+        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+            bool got = w.wait(smem_u32(&ctl->full_i8[si]), phi);
+            got = got && w.wait(smem_u32(&ctl->empty[sf]), phf ^ 1u);
+            if (!__all_sync(0xffffffffu, got)) return;
+            const uint32_t ia = sbase + Cfg::I8_OFF + si * Cfg::I8_STAGE_BYTES;
+            const uint32_t ib = ia + Cfg::I8_A_BYTES;
+            const uint32_t fa = sbase + sf * Cfg::STAGE_BYTES;
+            const uint32_t fb = fa + Cfg::A_BYTES;
+            constexpr int NA = A_PIECES / Cfg::CONV_THREADS, NB = B_PIECES / Cfg::CONV_THREADS;
+            // All shared loads of the k-block first (they pipeline), then the
+            // widening and the stores.
+            uint4 va[NA], vb[NB];
+#pragma unroll
+            for (int i = 0; i < NA; ++i) {
+                const int pc = ct + i * Cfg::CONV_THREADS;
+                va[i] = ld_shared_v4(ia + (pc >> 2) * 64 + (pc & 3) * 16);
+            }
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                const int pc = ct + i * Cfg::CONV_THREADS;
+                vb[i] = ld_shared_v4(ib + (pc / B_ROW_PIECES) * Cfg::BN + (pc % B_ROW_PIECES) * 16);
+            }
+#pragma unroll
+            for (int i = 0; i < NA; ++i) {
+                const int pc = ct + i * Cfg::CONV_THREADS;
+                const int r = pc >> 2, j = pc & 3;  // row, 16-k piece of the 64-k row
+                const uint32_t row = fa + r * 128;
+                widen16_store(va[i], row + (((2 * j) ^ (r & 7)) << 4), row + (((2 * j + 1) ^ (r & 7)) << 4));
+            }
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                const int pc = ct + i * Cfg::CONV_THREADS;
+                const int kk = pc / B_ROW_PIECES, jn = pc % B_ROW_PIECES;  // k row, 16-n piece
+                if (jn * 16 < bn) {
+                    const uint32_t row = fb + (jn >> 2) * 8192 + kk * 128;
+                    const int c0 = (jn & 3) * 2;
+                    widen16_store(vb[i], row + ((c0 ^ (kk & 7)) << 4), row + (((c0 + 1) ^ (kk & 7)) << 4));
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&ctl->full[sf]));
+            mbar_arrive(smem_u32(&ctl->empty_i8[si]));
+            if (++si == Cfg::I8_STAGES) {
+                si = 0;
+                phi ^= 1u;
+            }
+            if (++sf == Cfg::STAGES) {
+                sf = 0;
+                phf ^= 1u;
+            }
+        }
+    }
+}
+
+template <class Cfg>
 __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
-                             uint32_t sbase, Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+                             uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
     int stage = 0;
     uint32_t phase = 0;
@@ -261,7 +419,7 @@ __device__ __forceinline__ void seg_store(const SegLoad &r, int j, uint32_t dst)
 }
 
 template <class Cfg>
-__device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+__device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
     constexpr int GROUPS = Cfg::PRODUCER_THREADS / 8;  // row segments per pass
     constexpr int SEGS = Cfg::BM + Cfg::BK * Cfg::NB64;
@@ -331,7 +489,7 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
 
 template <class Cfg>
 __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
-                           Ctl<Cfg::STAGES> *ctl, const Waiter &w)
+                           Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
     constexpr uint32_t IDESC_FULL = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
     constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(Cfg::BM, Cfg::BN / 2, true);
@@ -389,6 +547,7 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
 // columns col0 .. col0 + 31.  The block goes through the warp's staging tile
 // (16-byte chunks XOR-swizzled by row, conflict-free both ways) so that each
 // global store instruction writes whole 128-byte row pieces.
+template <bool ADD = false>
 __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, const uint32_t *r,
                                             int64_t row0, int64_t col0, int lane)
 {
@@ -408,11 +567,16 @@ __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, c
             if (grow < p.M && gcol < p.N) {
                 uint32_t *dst = C + grow * p.ldc + gcol;
                 if (gcol + 4 <= p.N) {
-                    *reinterpret_cast<uint4 *>(dst) = v;
+                    if constexpr (ADD) {
+                        const uint4 o = *reinterpret_cast<const uint4 *>(dst);
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+                    } else {
+                        *reinterpret_cast<uint4 *>(dst) = v;
+                    }
                 } else {
-                    dst[0] = v.x;
-                    if (gcol + 1 < p.N) dst[1] = v.y;
-                    if (gcol + 2 < p.N) dst[2] = v.z;
+                    dst[0] = ADD ? dst[0] + v.x : v.x;
+                    if (gcol + 1 < p.N) dst[1] = ADD ? dst[1] + v.y : v.y;
+                    if (gcol + 2 < p.N) dst[2] = ADD ? dst[2] + v.z : v.z;
                 }
             }
         }
@@ -421,14 +585,14 @@ __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, c
         for (int rr = 0; rr < 32; ++rr) {
             const uint32_t v = ld_shared_b32(stg + rr * 128 + ((((lane >> 2) ^ (rr & 7))) << 4) + ((lane & 3) << 2));
             const int64_t grow = row0 + rr, gcol = col0 + lane;
-            if (grow < p.M && gcol < p.N) C[grow * p.ldc + gcol] = v;
+            if (grow < p.M && gcol < p.N) C[grow * p.ldc + gcol] = ADD ? C[grow * p.ldc + gcol] + v : v;
         }
     }
     __syncwarp();
 }
 
 template <class Cfg>
-__device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES> *ctl,
+__device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
                          const Waiter &w, int warp, int lane)
 {
     const int e = warp - Cfg::EPI_WARP0;  // 0..7
@@ -441,8 +605,8 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
         const int ncols = tk.bn / 2;  // this warp's columns
         const int64_t row0 = tk.m0 + q * 32;
         const int64_t colb = tk.n0 + h * ncols;
-        uint32_t isum[Cfg::INT_OUT ? Cfg::EPI_COLS : 1];
-        if constexpr (Cfg::INT_OUT) {
+        uint32_t isum[(Cfg::INT_OUT && !Cfg::CONVERT) ? Cfg::EPI_COLS : 1];
+        if constexpr (Cfg::INT_OUT && !Cfg::CONVERT) {
 #pragma unroll
             for (int i = 0; i < Cfg::EPI_COLS; ++i) isum[i] = 0;
         }
@@ -451,7 +615,26 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             if (!__all_sync(0xffffffffu, got)) return;
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * ncols;
-            if constexpr (Cfg::INT_OUT) {
+            if constexpr (Cfg::CONVERT) {
+                // Chunk partials are exact integers; the first chunk stores
+                // them, later chunks add into C (each element is read and
+                // written by the same thread, in chunk order).
+#pragma unroll
+                for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
+                    if (jb < ncols / 32) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+                        if (kc == 0)
+                            store_block<false>(p, stg, r, row0, colb + jb * 32, lane);
+                        else
+                            store_block<true>(p, stg, r, row0, colb + jb * 32, lane);
+                    }
+                }
+            } else if constexpr (Cfg::INT_OUT) {
                 // Chunk partials are integers below 2^24 in magnitude: exact
                 // in fp32, so the conversion is exact.  16 columns per load
                 // keep the 128 running sums in registers.
@@ -483,7 +666,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if constexpr (Cfg::INT_OUT) {
+        if constexpr (Cfg::INT_OUT && !Cfg::CONVERT) {
 #pragma unroll
             for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb)
                 if (jb < ncols / 32) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
@@ -503,13 +686,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
-    auto *ctl = reinterpret_cast<Ctl<Cfg::STAGES> *>(smem + Cfg::CTL_OFF);
+    auto *ctl = reinterpret_cast<Ctl<Cfg::STAGES, Cfg::I8_STAGES> *>(smem + Cfg::CTL_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), Cfg::LDG ? Cfg::PRODUCER_THREADS : 1);
+            mbar_init(smem_u32(&ctl->full[s]),
+                      Cfg::LDG ? Cfg::PRODUCER_THREADS : (Cfg::CONVERT ? Cfg::CONV_THREADS : 1));
             mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int s = 0; s < Cfg::I8_STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full_i8[s]), 1);
+            mbar_init(smem_u32(&ctl->empty_i8[s]), Cfg::CONV_THREADS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -538,9 +726,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp < Cfg::PRODUCER_WARPS) {
         if constexpr (Cfg::LDG) {
             producer_ldg<Cfg>(p, sbase, ctl, w);
+        } else if constexpr (Cfg::CONVERT) {
+            if (lane == 0) producer_tma_i8<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
         } else {
             if (lane == 0) producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
         }
+    } else if (warp < Cfg::MMA_WARP) {
+        if constexpr (Cfg::CONVERT) converter<Cfg>(p, sbase, ctl, w);
     } else if (warp == Cfg::MMA_WARP) {
         if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
         __syncwarp();

@@ -4,8 +4,10 @@
 namespace gp {
 
 static const Variant kS8Variants[] = {
-    make_variant<GemmCfg<256, 4, false, true>>(),
+    make_variant<GemmCfg<256, 4, false, true>>(),  // fp16-widened operands from the workspace
     make_variant<GemmCfg<128, 6, false, true>>(),
+    make_variant<GemmCfg<256, 2, false, true, true, 4>>(),  // int8 TMA + in-kernel widening
+    make_variant<GemmCfg<128, 3, false, true, true, 6>>(),
 };
 
 int variants_s8(const Variant **out)

@@ -131,34 +131,52 @@ struct Plan {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-const Variant *find_variant(int int_out, int producer, int bn, int stages)
+const Variant *find_variant(int int_out, int convert, int producer, int bn, int stages)
 {
     const Variant *tab = nullptr;
     const int n = int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
     for (int i = 0; i < n; ++i) {
         const gp::VariantInfo &f = tab[i].info;
-        if (f.producer == producer && f.BN == bn && (stages == 0 || f.stages == stages)) return &tab[i];
+        if (f.producer == producer && f.convert == convert && f.BN == bn && (stages == 0 || f.stages == stages))
+            return &tab[i];
     }
     return nullptr;
 }
 
-// The plan for an fp16-operand GEMM (INT8 calls pass their widened copies).
+// INT8 operands the converter variant can take straight from the caller:
+// TMA needs 16-byte aligned bases and row pitches (K and N multiples of 16
+// int8).  It is taken only when asked for (producer override 0): widening
+// inside the kernel redoes the conversion of every operand tile for every
+// output tile that reads it, which costs more shared-memory bandwidth than
+// one widening pass over the operands.
+bool s8_convert_ok(const void *A, int64_t K, const void *B, int64_t N)
+{
+    if (!(aligned16(A) && aligned16(B) && K % 16 == 0 && N % 16 == 0)) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_override.producer == 0;
+}
+
+// The plan of one GEMM.  fp16 operands (or INT8 calls' widened copies) when
+// convert is false; int8 operands read by TMA and widened in the kernel when
+// convert is true.
 gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
-                            const void *B, int64_t ldb, const void *C, int64_t ldc, const DeviceInfo &d, Plan *pl)
+                            const void *B, int64_t ldb, const void *C, int64_t ldc, const DeviceInfo &d, Plan *pl,
+                            bool convert = false)
 {
     Override ov;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         ov = g_override;
     }
-    const bool tma_ok = aligned16(A) && aligned16(B) && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0;
+    const int esz = convert ? 1 : 2;
+    const bool tma_ok = aligned16(A) && aligned16(B) && (lda * esz) % 16 == 0 && (ldb * esz) % 16 == 0;
     int producer = tma_ok ? 0 : 1;
     if (ov.producer == 1) producer = 1;
     if (int_out) producer = 0;  // widened operands are always TMA-describable
     int bn = N <= 128 ? 128 : 256;
     if (ov.bn) bn = ov.bn;
-    const Variant *v = find_variant(int_out, producer, bn, ov.stages);
-    if (!v) v = find_variant(int_out, producer, bn, 0);
+    const Variant *v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages);
+    if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, 0);
     if (!v) return GEMMPIPE_ERR_INTERNAL;
     if (v->info.smem_bytes > d.smem_optin) return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
     pl->v = v;
@@ -205,19 +223,28 @@ EncodeFn encode_fn()
     return f;
 }
 
-// 2-D fp16 tensor (rows x cols, pitch `ld` elements), 128-byte swizzle,
-// box = 64 columns x box_rows rows, zero fill outside the tensor.
-bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+// 2-D row-major tensor (rows x cols, pitch `ld` elements), zero fill
+// outside it.  fp16: 128-byte swizzle, box 64 columns x box_rows rows.
+// int8: no swizzle, box box_cols x box_rows.
+bool encode_2d_any(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                   int box_rows, bool int8)
 {
     EncodeFn f = encode_fn();
     if (!f) return false;
+    const int esz = int8 ? 1 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esz)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return f(m, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows)
+{
+    return encode_2d_any(m, base, rows, cols, ld, 64, box_rows, false);
 }
 
 // ------------------------------------------------------------------ timing
@@ -303,7 +330,11 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
-    if (pl.v->info.producer == 0) {
+    if (pl.v->info.convert) {
+        if (!encode_2d_any(&ta, A, M, K, lda, kBK, kBM, true) ||
+            !encode_2d_any(&tb, B, K, N, ldb, pl.v->info.BN, kBK, true))
+            return GEMMPIPE_ERR_INTERNAL;
+    } else if (pl.v->info.producer == 0) {
         if (!encode_2d(&ta, A, M, K, lda, kBM) || !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
     }
     GemmParams p;
@@ -508,6 +539,14 @@ gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A,
     if ((st = check_device_pointers(K, A, B, C, 1, 4)) != GEMMPIPE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, M * N * 4, d, s);
+    if (s8_convert_ok(A, K, B, N)) {
+        // int8 tiles straight from A and B, widened inside the kernel.
+        Plan pl;
+        const uint16_t *A8 = reinterpret_cast<const uint16_t *>(A);
+        const uint16_t *B8 = reinterpret_cast<const uint16_t *>(B);
+        if ((st = make_plan(true, M, N, K, A8, K, B8, N, C, N, d, &pl, true)) != GEMMPIPE_OK) return st;
+        return run_plan(pl, true, M, N, K, A8, K, B8, N, C, N, s);
+    }
     const int64_t Kp = round8(K), Np = round8(N);
     void *ws = nullptr;
     if ((st = workspace(dev, s, s8_workspace_bytes(M, N, K), &ws)) != GEMMPIPE_OK) return st;
@@ -596,9 +635,13 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     std::memset(plan, 0, sizeof(*plan));
     if (M == 0 || N == 0 || K == 0) return GEMMPIPE_OK;
     Plan pl;
-    if (s8) {
+    if (s8 && s8_convert_ok(A, K, B, N)) {
+        st = make_plan(true, M, N, K, A, K, B, N, C, N, d, &pl, true);
+    } else if (s8) {
         // The widened copies are 16-byte aligned with 16-byte row pitches.
         st = make_plan(true, M, N, K, kAligned, round8(K), kAligned, round8(N), C, N, d, &pl);
+        plan->workspace_bytes = s8_workspace_bytes(M, N, K);
+        plan->operand_copy = 1;
     } else if (pad_wanted(A, K, B, N)) {
         const bool pa = !operand_tma_ok(A, K), pb = !operand_tma_ok(B, N);
         st = make_plan(false, M, N, K, pa ? kAligned : A, pa ? round8(K) : K, pb ? kAligned : B,
@@ -623,10 +666,7 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     plan->k_blocks = pl.num_kb;
     plan->smem_bytes = f.smem_bytes;
     plan->vector_store = pl.vec_store;
-    if (s8) {
-        plan->workspace_bytes = s8_workspace_bytes(M, N, K);
-        plan->operand_copy = 1;
-    }
+
     return GEMMPIPE_OK;
 }
 

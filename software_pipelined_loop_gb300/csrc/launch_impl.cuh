@@ -29,8 +29,8 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmPar
 template <class Cfg>
 constexpr Variant make_variant()
 {
-    return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK, Cfg::STAGES, Cfg::THREADS,
-                    Cfg::SMEM_BYTES},
+    return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::CONVERT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK,
+                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::THREADS, Cfg::SMEM_BYTES},
                    &launch_cfg<Cfg>};
 }
 

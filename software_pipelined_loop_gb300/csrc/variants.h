@@ -12,7 +12,9 @@ namespace gp {
 struct VariantInfo {
     int producer;  // 0 TMA, 1 bounded loads
     int int_out;   // 1: INT8 chunked integer epilogue
+    int convert;   // 1: int8 tiles by TMA, widened to fp16 in shared memory
     int BM, BN, BK, stages;
+    int i8_stages;
     int threads;
     int smem_bytes;
 };

@@ -196,19 +196,33 @@ def test_host_pointer_rejected(dev):
 
 # ----------------------------------------------------------- INT8 exactness
 
-@pytest.mark.parametrize("K", [1024, 1025, 2048, 3000, 4096])
-def test_s8_chunk_exactness_extremes(dev, K):
+@pytest.mark.parametrize("forced", [-1, 0], ids=["widened_in_workspace", "widened_in_kernel_if_aligned"])
+@pytest.mark.parametrize("N", [264, 272])
+@pytest.mark.parametrize("K", [1024, 1025, 2048, 3000, 4096, 4112])
+def test_s8_chunk_exactness_extremes(dev, K, N, forced):
     # Products of +-127/-128 make every chunk partial an odd or large integer
     # near 2^24 in magnitude: any bit the fp32 accumulation dropped shows.
-    M, N = 130, 264
+    # N = 264 is not a multiple of 16 (workspace path); N = 272 with K a
+    # multiple of 16 takes the in-kernel widening path.
+    M = 130
     rng = np.random.default_rng(K)
     A = rng.choice(np.array([-128, 127, -127], dtype=np.int8), size=(M, K))
     B = rng.choice(np.array([-128, 127, 127], dtype=np.int8), size=(K, N))
+    expect_convert = (N % 16 == 0 and K % 16 == 0 and forced == 0)
+    gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
+    try:
+        assert gemmpipe.gemmpipe_plan(0, M, N, K)["operand_copy"] == (0 if expect_convert else 1)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     A[0, :] = 127
     B[:, 0] = 127          # C[0,0] = 16129 K: odd partials just below 2^24
     A[1, :] = -128
     B[:, 1] = -128         # C[1,1] = 16384 K: the chunk bound itself
-    got = run_s8(A, B, dev)
+    gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
+    try:
+        got = run_s8(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     want = oracle.gemm_s8s8s32(A, B)
     assert np.array_equal(got, want)
     assert got[0, 0] == 16129 * K and got[1, 1] == 16384 * K
@@ -301,17 +315,22 @@ def test_kernel_timing_and_launch_count(dev):
     A, B = inputs.make_operands("s8", M, N, K, seed=15)
     Ad, Bd = to_dev(A, dev), to_dev(B, dev)
     C = torch.zeros((M, N), dtype=torch.int32, device=dev)
-    n0 = gemmpipe.gemmpipe_launch_count()
-    gemmpipe.gemmpipe_timing_enable(True)
-    try:
-        for _ in range(3):
-            gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C)
-        gms, gn, ams, an = gemmpipe.gemmpipe_timing_read()
-    finally:
-        gemmpipe.gemmpipe_timing_enable(False)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
-    assert gn == 3 and an == 3 and gms > 0 and ams > 0
-    assert gemmpipe.gemmpipe_launch_count() - n0 == 6
+    gemmpipe.gemmpipe_timing_read()
+    for forced, aux in ((0, 0), (-1, 3)):   # in-kernel widening: 1 kernel; workspace path: 2 per call
+        gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
+        n0 = gemmpipe.gemmpipe_launch_count()
+        gemmpipe.gemmpipe_timing_enable(True)
+        try:
+            for _ in range(3):
+                gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C)
+            gms, gn, ams, an = gemmpipe.gemmpipe_timing_read()
+        finally:
+            gemmpipe.gemmpipe_timing_enable(False)
+            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+        assert gn == 3 and an == aux and gms > 0 and (ams > 0) == (aux > 0)
+        assert gemmpipe.gemmpipe_launch_count() - n0 == 3 + aux
+        assert np.array_equal(C.cpu().numpy(), oracle.gemm_s8s8s32(A, B))
 
 
 def test_copy_kernel(dev):
@@ -331,17 +350,20 @@ def test_copy_kernel(dev):
 
 @pytest.mark.parametrize("dtype", ["f16", "s8"])
 @pytest.mark.parametrize("wide", [True, False], ids=["bn256", "bn128"])
-def test_tail_wave_split(dev, dtype, wide):
+@pytest.mark.parametrize("n_extra", [0, 8], ids=["n16", "n8"])
+def test_tail_wave_split(dev, dtype, wide, n_extra):
     # Tile counts a little above one wave of the persistent grid: the tiles of
     # the last, partial wave run as two half-width tasks each.
     G = gemmpipe.gemmpipe_plan(1, 4096, 4096, 4096)["grid"]
     target = G + max(1, G // 4)
+    # n_extra = 0: N and K multiples of 16 (INT8 widened in the kernel);
+    # n_extra = 8: N only a multiple of 8 (INT8 widened in the workspace).
     if wide:
-        n_tiles, N = 2, 504
-        K = 136
+        n_tiles, N = 2, 496 + n_extra
+        K = 144
     else:
-        n_tiles, N = 1, 120
-        K = 200
+        n_tiles, N = 1, 112 + n_extra
+        K = 208
     m_tiles = -(-target // n_tiles)
     M = m_tiles * 128 - 5
     plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
@@ -366,3 +388,38 @@ def test_workload_fp16_4096_sampled(dev):
     got = run_f16(A, B, dev)
     rows = sample_rows(M)
     assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "fp16 4096^3")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 272, 1040), (129, 512, 2048), (1000, 256, 4096),
+                                   (64, 16, 16), (513, 144, 3088)])
+def test_s8_in_kernel_and_workspace_widening_agree(dev, M, N, K):
+    A, B = inputs.make_operands("s8", M, N, K, seed=600 + M + N + K)
+    want = oracle.gemm_s8s8s32(A, B)
+    assert gemmpipe.gemmpipe_plan(0, M, N, K)["operand_copy"] == 1
+    assert np.array_equal(run_s8(A, B, dev), want)
+    gemmpipe.gemmpipe_set_plan_override(0, 0, 0)
+    try:
+        assert gemmpipe.gemmpipe_plan(0, M, N, K)["operand_copy"] == 0
+        got = run_s8(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert np.array_equal(got, want)
+
+
+def test_s8_stall_times_out_in_converter_variant(dev):
+    import torch
+    M, N, K = 256, 256, 2048
+    A, B = inputs.make_operands("s8", M, N, K, seed=16)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.int32, device=dev)
+    gemmpipe.gemmpipe_set_plan_override(0, 0, 0)
+    try:
+        assert gemmpipe.gemmpipe_plan(0, M, N, K, Ad, Bd, C)["operand_copy"] == 0
+        gemmpipe.gemmpipe_test_inject_stall(5, 200)
+        gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+        gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert np.array_equal(C.cpu().numpy(), oracle.gemm_s8s8s32(A, B))
