@@ -197,10 +197,11 @@ GEMMPIPE_API int64_t gemmpipe_stage_smem_bytes(int BM, int BN, int BK, int elem_
 /* Kernel plan chosen for one call; filled by gemmpipe_plan(). */
 typedef struct {
     int producer;        /* 0: TMA producer warp, 1: bounded-load (LDG) producer warps */
-    int BM, BN, BK;      /* output tile and k-block */
+    int BM, BN, BK;      /* output tile (BM = 256 for a CTA pair) and k-block */
     int stages;          /* depth S of the shared-memory ring */
     int k_chunk;         /* k values accumulated in one TMEM accumulator before a drain */
     int threads;         /* threads per CTA */
+    int cta_pair;        /* 1: clusters of two CTAs share one 256-row MMA (tcgen05 cta_group::2) */
     int grid;            /* persistent CTAs launched */
     int64_t tiles;       /* output tiles of BM x BN */
     int64_t tasks;       /* work items: tiles, with the last partial wave split into BN/2-wide halves */
@@ -231,7 +232,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * in-kernel widening of int8 tiles), 1 bounded-load producer for
  * gemm_f16f32 and the workspace-widening path for gemm_s8s8s32.  bn: 0
  * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
- * depths (see gemmpipe_plan for what was taken).  Returns INVALID_VALUE for
+ * depths (a depth only a single-CTA variant has, such as 4 for 256-wide
+ * tiles, also selects single CTAs over CTA pairs; see gemmpipe_plan for what
+ * was taken).  Returns INVALID_VALUE for
  * values outside these sets.
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages);

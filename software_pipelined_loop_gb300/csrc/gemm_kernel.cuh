@@ -44,7 +44,8 @@ namespace gp {
 
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
-template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1>
+template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1,
+          bool PAIR_ = false>
 struct GemmCfg {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -53,10 +54,17 @@ struct GemmCfg {
     static constexpr bool LDG = LDG_;
     static constexpr bool INT_OUT = INT_OUT_;
 
+    // PAIR: a cluster of two CTAs computes a 256 x BN tile with one
+    // tcgen05.mma.cta_group::2 stream; each CTA holds 128 rows of A and
+    // BN/2 columns of B, and receives its 128 rows of the accumulator.
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+    static constexpr int CTA_BN = PAIR ? BN / 2 : BN;
+
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int B_BYTES = BK * CTA_BN * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int NB64 = BN / 64;  // 64-column B atoms per stage
+    static constexpr int NB64 = CTA_BN / 64;  // 64-column B atoms per stage
 
     // CONVERT: int8 operands arrive by TMA in an int8 ring; converter warps
     // widen them to fp16 into the MMA's stage (INT8 path without a widening
@@ -89,6 +97,7 @@ struct GemmCfg {
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
+    static_assert(!PAIR || (BN == 256 && !LDG && !CONVERT), "pair variant: TMA producer, 256-wide tiles");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
 };
@@ -155,11 +164,24 @@ template <class Cfg>
 __device__ __forceinline__ Task task_of(const GemmParams &p, int64_t u)
 {
     if (u < p.full_tasks) {
-        return Task{(u % p.m_tiles) * Cfg::BM, (u / p.m_tiles) * Cfg::BN, Cfg::BN};
+        return Task{(u % p.m_tiles) * Cfg::TILE_M, (u / p.m_tiles) * Cfg::BN, Cfg::BN};
     }
     const int64_t h = u - p.full_tasks;
     const int64_t t = p.full_tasks + (h >> 1);
-    return Task{(t % p.m_tiles) * Cfg::BM, (t / p.m_tiles) * Cfg::BN + (h & 1) * (Cfg::BN / 2), Cfg::BN / 2};
+    return Task{(t % p.m_tiles) * Cfg::TILE_M, (t / p.m_tiles) * Cfg::BN + (h & 1) * (Cfg::BN / 2), Cfg::BN / 2};
+}
+
+// Persistent schedule: a CTA (or a CTA pair) takes tasks first, first+step, ...
+template <class Cfg>
+__device__ __forceinline__ int64_t first_task()
+{
+    return Cfg::PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+}
+
+template <class Cfg>
+__device__ __forceinline__ int64_t task_step()
+{
+    return Cfg::PAIR ? (gridDim.x >> 1) : gridDim.x;
 }
 
 // ------------------------------------------------------------ TMA producer
@@ -175,7 +197,7 @@ __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, cons
     uint32_t armed = 0, armed_par = 0;
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
         const Task tk = task_of<Cfg>(p, u);
         const int32_t m0 = static_cast<int32_t>(tk.m0);
         const int32_t n0 = static_cast<int32_t>(tk.n0);
@@ -251,7 +273,7 @@ __device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, 
     static_assert(A_PIECES % Cfg::CONV_THREADS == 0 && B_PIECES % Cfg::CONV_THREADS == 0, "even split");
     int si = 0, sf = 0;
     uint32_t phi = 0, phf = 0;
-    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
         const int bn = task_of<Cfg>(p, u).bn;
         for (int64_t kb = 0; kb < p.num_kb; ++kb) {
             bool got = w.wait(smem_u32(&ctl->full_i8[si]), phi);
@@ -316,7 +338,7 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
     uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arm
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
         const Task tk = task_of<Cfg>(p, u);
         const int32_t m0 = static_cast<int32_t>(tk.m0);
         const int32_t n0 = static_cast<int32_t>(tk.n0);
@@ -435,7 +457,7 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
     uint32_t phase = 0;
     int64_t kb_count = 0;
     // The host gives this producer whole tiles only (full_tasks == tasks).
-    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
         const Task tk = task_of<Cfg>(p, u);
         const int64_t m0 = tk.m0;
         const int64_t n0 = tk.n0;
@@ -485,6 +507,125 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
     }
 }
 
+// ------------------------------------------------------ pair (cta_group::2)
+//
+// Both CTAs of the pair run this producer.  Each loads its 128 rows of A and
+// its half of the task's B columns into its own stage; every copy counts its
+// bytes on the leader CTA's full[s], which the leader's producer arms with
+// the bytes of both CTAs.  empty[s] of each CTA is released by the leader's
+// multicast commit.
+template <class Cfg>
+__device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
+                                  uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w,
+                                  uint32_t rank)
+{
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_par = 0;
+    int64_t kb_count = 0;
+    bool ok = true;
+    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
+        const Task tk = task_of<Cfg>(p, u);
+        const int32_t m0 = static_cast<int32_t>(tk.m0 + rank * Cfg::BM);
+        const int half = tk.bn / 2;  // B columns this CTA loads
+        const int32_t n0 = static_cast<int32_t>(tk.n0 + rank * half);
+        const int natoms = half / 64;
+        const uint32_t pair_bytes = 2u * (Cfg::A_BYTES + half * Cfg::BK * 2);
+        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+            if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) {
+                const uint32_t fb_local = smem_u32(&ctl->full[stage]);
+                const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's full[s]
+                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
+                const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
+                if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
+                tma_load_2d_pair(sa, tA, fb, k0, m0);
+#pragma unroll
+                for (int j = 0; j < Cfg::NB64; ++j)
+                    if (j < natoms) tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                armed |= 1u << stage;
+                armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
+            }
+            if (++stage == Cfg::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        if (rank == 0) {
+            // The leader's full barriers count both CTAs' copies.
+            for (int s = 0; s < Cfg::STAGES; ++s)
+                if (armed & (1u << s))
+                    w.wait_drain(smem_u32(&ctl->full[s]), (armed_par >> s) & 1u, kDrainNs);
+        } else if (armed) {
+            // The peer cannot observe its copies (they count on the leader's
+            // barriers): give them a bounded time to land.
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 2000000ull) {
+            }
+        }
+    }
+}
+
+// Leader CTA only: one thread issues the pair's MMAs.
+template <class Cfg>
+__device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
+                                Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
+{
+    constexpr uint32_t IDESC_FULL = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN, true);
+    constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN / 2, true);
+    constexpr uint16_t BOTH = 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
+    bool issued = false, ok = true;
+    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
+        const uint32_t idesc = task_of<Cfg>(p, u).bn == Cfg::BN ? IDESC_FULL : IDESC_HALF;
+        for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
+            const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
+            if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d = tmem_base + acc * Cfg::BN;
+            for (int64_t kb = kc; kb < kend; ++kb) {
+                if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
+                const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
+                    const uint64_t da = umma_desc_sw128(sa + kk * 32, 16, 1024);
+                    const uint64_t db = umma_desc_sw128(sb + kk * 2048, 8192, 1024);
+                    umma_f16_pair(d, da, db, idesc, (kb > kc || kk > 0) ? 1u : 0u);
+                }
+                issued = true;
+                umma_commit_pair(smem_u32(&ctl->empty[stage]), BOTH);
+                if (++stage == Cfg::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair(smem_u32(&ctl->tfull[acc]), BOTH);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    if (!ok && issued) {
+        umma_commit_pair(smem_u32(&ctl->drain), 1);
+        w.wait_drain(smem_u32(&ctl->drain), 0, kDrainNs);
+    }
+}
+
 // ------------------------------------------------------------- MMA issuer
 
 template <class Cfg>
@@ -497,7 +638,7 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
-    for (int64_t u = blockIdx.x; u < p.tasks && ok; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
         const uint32_t idesc = task_of<Cfg>(p, u).bn == Cfg::BN ? IDESC_FULL : IDESC_HALF;
         for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
             const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
@@ -593,17 +734,17 @@ __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, c
 
 template <class Cfg>
 __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
-                         const Waiter &w, int warp, int lane)
+                         const Waiter &w, int warp, int lane, uint32_t rank)
 {
     const int e = warp - Cfg::EPI_WARP0;  // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int h = e >> 2;                  // column half of the tile
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t u = blockIdx.x; u < p.tasks; u += gridDim.x) {
+    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
         const Task tk = task_of<Cfg>(p, u);
         const int ncols = tk.bn / 2;  // this warp's columns
-        const int64_t row0 = tk.m0 + q * 32;
+        const int64_t row0 = tk.m0 + rank * Cfg::BM + q * 32;
         const int64_t colb = tk.n0 + h * ncols;
         uint32_t isum[(Cfg::INT_OUT && !Cfg::CONVERT) ? Cfg::EPI_COLS : 1];
         if constexpr (Cfg::INT_OUT && !Cfg::CONVERT) {
@@ -662,7 +803,12 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            if (lane == 0) {
+                if constexpr (Cfg::PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));  // the leader's
+                else
+                    mbar_arrive(smem_u32(&ctl->tempty[acc]));
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -701,15 +847,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tfull[b]), 1);
-            mbar_init(smem_u32(&ctl->tempty[b]), Cfg::EPI_WARPS);
+            mbar_init(smem_u32(&ctl->tempty[b]), (Cfg::PAIR ? 2 : 1) * Cfg::EPI_WARPS);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
         fence_mbar_init();
     }
     if (warp == Cfg::MMA_WARP) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (Cfg::PAIR) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if constexpr (!Cfg::LDG) {
         if (threadIdx.x == 0) {
@@ -719,32 +870,44 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (Cfg::PAIR) cluster_sync();  // the leader's barriers exist before the peer signals them
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const Waiter w{&ctl->abort, p.status, p.timeout_ns};
+    const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
 
     if (warp < Cfg::PRODUCER_WARPS) {
         if constexpr (Cfg::LDG) {
             producer_ldg<Cfg>(p, sbase, ctl, w);
         } else if constexpr (Cfg::CONVERT) {
             if (lane == 0) producer_tma_i8<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
+        } else if constexpr (Cfg::PAIR) {
+            if (lane == 0) producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
         } else {
             if (lane == 0) producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
         }
     } else if (warp < Cfg::MMA_WARP) {
         if constexpr (Cfg::CONVERT) converter<Cfg>(p, sbase, ctl, w);
     } else if (warp == Cfg::MMA_WARP) {
-        if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+        if constexpr (Cfg::PAIR) {
+            if (lane == 0 && rank == 0) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w);
+        } else {
+            if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+        }
         __syncwarp();
     } else {
-        epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane);
+        epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane, rank);
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (Cfg::PAIR) cluster_sync();  // no peer still signals or reads this CTA
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (Cfg::PAIR)
+            tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

@@ -131,13 +131,14 @@ struct Plan {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-const Variant *find_variant(int int_out, int convert, int producer, int bn, int stages)
+const Variant *find_variant(int int_out, int convert, int producer, int bn, int stages, int pair)
 {
     const Variant *tab = nullptr;
     const int n = int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
     for (int i = 0; i < n; ++i) {
         const gp::VariantInfo &f = tab[i].info;
-        if (f.producer == producer && f.convert == convert && f.BN == bn && (stages == 0 || f.stages == stages))
+        if (f.producer == producer && f.convert == convert && f.BN == bn && f.pair == pair &&
+            (stages == 0 || f.stages == stages))
             return &tab[i];
     }
     return nullptr;
@@ -175,22 +176,33 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (int_out) producer = 0;  // widened operands are always TMA-describable
     int bn = N <= 128 ? 128 : 256;
     if (ov.bn) bn = ov.bn;
-    const Variant *v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages);
-    if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, 0);
+    // A CTA pair (256 x 256 tiles, cta_group::2 MMA) when both dimensions
+    // exceed one 128-row / 128-column tile and TMA reads the operands.
+    const Variant *v = nullptr;
+    if (producer == 0 && !convert && bn == 256 && M > kBM && N > 128) {
+        v = find_variant(int_out, 0, 0, 256, ov.stages, 1);
+        if (v && v->max_pairs() < 1) v = nullptr;
+    }
+    if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages, 0);
+    if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, 0, 0);
     if (!v) return GEMMPIPE_ERR_INTERNAL;
     if (v->info.smem_bytes > d.smem_optin) return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
     pl->v = v;
-    pl->m_tiles = (M + kBM - 1) / kBM;
+    const int64_t tile_m = v->info.pair ? 2 * kBM : kBM;
+    pl->m_tiles = (M + tile_m - 1) / tile_m;
     pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
-    pl->grid = static_cast<int>(pl->tiles < d.sms ? pl->tiles : d.sms);
+    // Persistent grid: one CTA (or CTA pair) per SM (pair) slot.
+    const int64_t slots = v->info.pair ? v->max_pairs() : d.sms;
+    const int64_t units = pl->tiles < slots ? pl->tiles : slots;
+    pl->grid = static_cast<int>(v->info.pair ? 2 * units : units);
     // Balance the last wave: if the tiles left after the full waves fit
     // twice over into the grid, each is done as two half-width tasks.
-    const int64_t rem = pl->tiles % pl->grid;
+    const int64_t rem = pl->tiles % units;
     pl->full_tasks = pl->tiles;
     pl->tasks = pl->tiles;
-    if (v->info.producer == 0 && rem > 0 && 2 * rem <= pl->grid && pl->tiles > pl->grid) {
+    if (v->info.producer == 0 && rem > 0 && 2 * rem <= units && pl->tiles > units) {
         pl->full_tasks = pl->tiles - rem;
         pl->tasks = pl->tiles + rem;
     }
@@ -335,6 +347,8 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
             !encode_2d_any(&tb, B, K, N, ldb, pl.v->info.BN, kBK, true))
             return GEMMPIPE_ERR_INTERNAL;
     } else if (pl.v->info.producer == 0) {
+        // Boxes: A 64 (k) x 128 rows, B 64 (n) x 64 (k); a pair CTA loads the
+        // same boxes for its half.
         if (!encode_2d(&ta, A, M, K, lda, kBM) || !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
     }
     GemmParams p;
@@ -654,7 +668,8 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     if (st != GEMMPIPE_OK) return st;
     const gp::VariantInfo &f = pl.v->info;
     plan->producer = f.producer;
-    plan->BM = f.BM;
+    plan->BM = f.pair ? 2 * f.BM : f.BM;
+    plan->cta_pair = f.pair;
     plan->BN = f.BN;
     plan->BK = f.BK;
     plan->stages = f.stages;

@@ -22,16 +22,77 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmPar
         if (e != cudaSuccess) return e;
         attr_done[dev].store(1);
     }
-    gemm_pipelined_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p);
-    return cudaGetLastError();
+    if constexpr (Cfg::PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemm_pipelined_kernel<Cfg>, a, b, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    } else {
+        gemm_pipelined_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p);
+        return cudaGetLastError();
+    }
+}
+
+// Number of CTA pairs of this variant the current device can hold at once
+// (0 on error or for single-CTA variants).
+template <class Cfg>
+int max_pairs_cfg()
+{
+    if constexpr (!Cfg::PAIR) {
+        return 0;
+    } else {
+        static std::atomic<int> cache[128];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+            cudaGetLastError();
+            return 0;
+        }
+        int n = cache[dev].load();
+        if (n > 0) return n;
+        if (cudaFuncSetAttribute(gemm_pipelined_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1), 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_pipelined_kernel<Cfg>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev].store(n);
+        return n;
+    }
 }
 
 template <class Cfg>
 constexpr Variant make_variant()
 {
     return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::CONVERT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK,
-                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::THREADS, Cfg::SMEM_BYTES},
-                   &launch_cfg<Cfg>};
+                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::PAIR ? 1 : 0, Cfg::THREADS, Cfg::SMEM_BYTES},
+                   &launch_cfg<Cfg>, &max_pairs_cfg<Cfg>};
 }
 
 }  // namespace gp

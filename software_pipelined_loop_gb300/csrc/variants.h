@@ -15,16 +15,19 @@ struct VariantInfo {
     int convert;   // 1: int8 tiles by TMA, widened to fp16 in shared memory
     int BM, BN, BK, stages;
     int i8_stages;
+    int pair;  // 1: cluster of two CTAs, tcgen05.mma.cta_group::2, 256-row tiles
     int threads;
     int smem_bytes;
 };
 
 using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const GemmParams &, int grid,
                                  cudaStream_t);
+using ClustersFn = int (*)();  // co-resident CTA pairs on the current device (pair variants)
 
 struct Variant {
     VariantInfo info;
     LaunchFn launch;
+    ClustersFn max_pairs;
 };
 
 // Each kernel translation unit exports its variants.

@@ -33,7 +33,7 @@ class GemmpipeError(RuntimeError):
 class PlanT(ctypes.Structure):
     _fields_ = [("producer", ctypes.c_int), ("BM", ctypes.c_int), ("BN", ctypes.c_int), ("BK", ctypes.c_int),
                 ("stages", ctypes.c_int), ("k_chunk", ctypes.c_int), ("threads", ctypes.c_int),
-                ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("tasks", ctypes.c_int64),
+                ("cta_pair", ctypes.c_int), ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("tasks", ctypes.c_int64),
                 ("k_blocks", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("vector_store", ctypes.c_int),
                 ("operand_copy", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]

@@ -353,29 +353,67 @@ def test_copy_kernel(dev):
 @pytest.mark.parametrize("n_extra", [0, 8], ids=["n16", "n8"])
 def test_tail_wave_split(dev, dtype, wide, n_extra):
     # Tile counts a little above one wave of the persistent grid: the tiles of
-    # the last, partial wave run as two half-width tasks each.
-    G = gemmpipe.gemmpipe_plan(1, 4096, 4096, 4096)["grid"]
-    target = G + max(1, G // 4)
-    # n_extra = 0: N and K multiples of 16 (INT8 widened in the kernel);
-    # n_extra = 8: N only a multiple of 8 (INT8 widened in the workspace).
+    # the last, partial wave run as two half-width tasks each.  Wide shapes
+    # run on CTA pairs (256-row tiles), N <= 128 on single CTAs.
     if wide:
-        n_tiles, N = 2, 496 + n_extra
-        K = 144
+        N, K, n_tiles = 496 + n_extra, 144, 2
     else:
-        n_tiles, N = 1, 112 + n_extra
-        K = 208
-    m_tiles = -(-target // n_tiles)
-    M = m_tiles * 128 - 5
+        N, K, n_tiles = 112 + n_extra, 208, 1
+    probe = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, 1 << 20, N, K)  # more tiles than slots
+    units = probe["grid"] // (2 if probe["cta_pair"] else 1)
+    tile_m = probe["BM"]
+    assert probe["cta_pair"] == (1 if wide else 0)
+    m_tiles = -(-(units + max(1, units // 4)) // n_tiles)
+    M = m_tiles * tile_m - 5
     plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
     tiles = m_tiles * n_tiles
-    rem = tiles % G
-    assert plan["tiles"] == tiles and plan["BN"] == (256 if wide else 128)
-    assert 0 < rem and 2 * rem <= G and plan["tasks"] == tiles + rem
+    rem = tiles % units
+    assert plan["tiles"] == tiles
+    assert 0 < rem and 2 * rem <= units and plan["tasks"] == tiles + rem
     A, B = inputs.make_operands(dtype, M, N, K, seed=500 + M)
     if dtype == "s8":
         assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
     else:
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (257, 264, 200), (1000, 776, 1032), (4093, 3000, 136),
+                                   (512, 136, 4096), (200, 1024, 64)])
+def test_cta_pair_matches_single_cta(dev, dtype, M, N, K):
+    # Default plan: CTA pairs (cta_group::2, 256-row tiles).  Stages = 4
+    # selects the single-CTA 128 x 256 variant.  Both must match the oracle.
+    A, B = inputs.make_operands(dtype, M, N, K, seed=700 + M + N + K)
+    want = oracle.gemm_s8s8s32(A, B) if dtype == "s8" else oracle.gemm_f16f32(A, B)
+    run = run_s8 if dtype == "s8" else run_f16
+    check = (lambda g: np.testing.assert_array_equal(g, want)) if dtype == "s8" else \
+        (lambda g: assert_f16_close(g, want))
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    assert plan["cta_pair"] == 1 and plan["BM"] == 256
+    check(run(A, B, dev))
+    gemmpipe.gemmpipe_set_plan_override(-1, 256, 4)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+        assert plan["cta_pair"] == 0 and plan["BM"] == 128
+        got = run(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    check(got)
+
+
+def test_cta_pair_stall_times_out(dev):
+    import torch
+    M, N, K = 512, 512, 1024
+    A, B = inputs.make_operands("f16", M, N, K, seed=17)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    assert gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)["cta_pair"] == 1
+    gemmpipe.gemmpipe_test_inject_stall(2, 200)
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
 def test_workload_fp16_4096_sampled(dev):
