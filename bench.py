@@ -40,6 +40,36 @@ FLUSH_BYTES = 256 << 20
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM bytes (read + write) per launch of a kernel variant, from one
+# `ncu --set full` capture (profiles/), valid only while the kernel sources
+# hash as they did when the counters were taken.
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu"]
+TRAFFIC = {
+    # (int8 operands, cta pair, BN): (bytes per launch, sources hash, profile)
+    ("s8", 1, 256): (116_392_192, "79745a44834dba15", "profiles/gemm_pair_int8_4096.md"),
+    ("f16", 1, 256): (117_359_360, "79745a44834dba15", "profiles/gemm_pair_f16_4096.md"),
+}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "software_pipelined_loop_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(dtype: str, plan: dict, shape: tuple) -> tuple[int | None, str | None]:
+    """Captured DRAM traffic of the 4096^3 launch this plan runs, or None."""
+    if shape != (4096, 4096, 4096):
+        return None, None
+    t = TRAFFIC.get((dtype, plan["cta_pair"], plan["BN"]))
+    if t is None or t[1] != kernel_source_hash():
+        return None, None
+    return t[0], t[2]
+
+
 def load_peaks() -> tuple[dict, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -52,7 +82,7 @@ def load_peaks() -> tuple[dict, str]:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples (20 Hz) with host timestamps; the bench asks for
+    """nvidia-smi samples (50 Hz) with host timestamps; the bench asks for
     the ones that fall inside its timed window."""
 
     QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -69,7 +99,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -91,7 +121,7 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float) -> dict:
-        win = [s for t, s in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        win = [s for t, s in self.samples if t0 - 0.025 <= t <= t1 + 0.025]
         if not win:
             win = [s for _, s in self.samples]
         sm = [float(s[0]) for s in win if s and s[0].replace(".", "").isdigit()]
@@ -232,9 +262,12 @@ def measure_gemm(wl, steps: int, warmup: int, dev, flush, peaks, peak_src):
     else:
         peak = peaks["bf16_tflops"]
         achieved = flops / kernel_ms / 1e9
+        traffic, prof = measured_traffic(dtype, plan, (M, N, K))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"bf16_tflops burst ({peak_src}); kind::f16 runs at the bf16 rate"}
+        if prof:
+            roof["traffic_source"] = prof
     return {
         "name": name, "dtype": dtype, "M": M, "N": N, "K": K, "ms": ms, "ms_median": statistics.median(times),
         "ops_per_s": flops / ms / 1e9, "bytes_per_s": alg_bytes / ms / 1e6, "kernel_ms": kernel_ms,
