@@ -45,7 +45,7 @@ namespace gp {
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
 template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1,
-          bool PAIR_ = false>
+          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4>
 struct GemmCfg {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -72,17 +72,24 @@ struct GemmCfg {
     static constexpr bool CONVERT = CONVERT_;
     static constexpr int I8_STAGES = CONVERT ? I8_STAGES_ : 0;
     static constexpr int I8_A_BYTES = BM * BK;
-    static constexpr int I8_B_BYTES = BK * BN;
+    static constexpr int I8_B_ATOMS = (PAIR_ ? BN_ / 2 : BN_) / 128;  // 128-column int8 atoms
+    static constexpr int I8_B_BYTES = BK * 128 * I8_B_ATOMS;
     static constexpr int I8_STAGE_BYTES = I8_A_BYTES + I8_B_BYTES;
 
     static constexpr int PRODUCER_WARPS = LDG ? 8 : 1;
     static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-    static constexpr int CONV_WARPS = CONVERT ? 4 : 0;
+    static constexpr int CONV_WARPS = CONVERT ? CONV_WARPS_ : 0;
     static constexpr int CONV_THREADS = 32 * CONV_WARPS;
+    static constexpr int CONV_GROUPS = CONV_GROUPS_;  // converter groups working on different k-blocks
+    static_assert(CONV_WARPS == 0 || CONV_WARPS % CONV_GROUPS == 0, "groups of whole warps");
     static constexpr int MMA_WARP = PRODUCER_WARPS + CONV_WARPS;
     static constexpr int EPI_WARP0 = MMA_WARP + 1;
     static constexpr int EPI_WARPS = 8;
     static constexpr int THREADS = 32 * (PRODUCER_WARPS + CONV_WARPS + 1 + EPI_WARPS);
+    // Running int32 sums of the INT8 chunks: in registers (128 per epilogue
+    // thread) while the CTA has at most 12 warps -- 3 per scheduler, 168
+    // registers each; with more warps they are kept in C itself.
+    static constexpr bool SUM_IN_C = CONVERT && THREADS > 12 * 32;
     static constexpr int EPI_COLS = BN / 2;  // columns per epilogue warp
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 
@@ -97,7 +104,8 @@ struct GemmCfg {
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
-    static_assert(!PAIR || (BN == 256 && !LDG && !CONVERT), "pair variant: TMA producer, 256-wide tiles");
+    static_assert(!PAIR || (BN == 256 && !LDG), "pair variant: TMA producer, 256-wide tiles");
+    static_assert(!CONVERT || I8_B_ATOMS >= 1, "int8 B atoms are 128 columns wide");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
 };
@@ -190,8 +198,11 @@ template <class Cfg>
 __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
                                 uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
-    // int8 tiles: A box 64 (k) x 128 (rows), B box BN (n) x 64 (k), no
-    // swizzle; always the whole box (half-width tasks convert half of B).
+    // int8 tiles into this CTA's int8 ring: A box 64 (k) x 128 (rows), no
+    // swizzle; B as atoms of 128 (n) x 64 (k) with the 128-byte swizzle.
+    // Always whole boxes (half-width tasks widen only the columns they use).
+    // In a CTA pair each CTA loads its own rows of A and half of B.
+    const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_par = 0;
@@ -199,8 +210,8 @@ __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, cons
     bool ok = true;
     for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
         const Task tk = task_of<Cfg>(p, u);
-        const int32_t m0 = static_cast<int32_t>(tk.m0);
-        const int32_t n0 = static_cast<int32_t>(tk.n0);
+        const int32_t m0 = static_cast<int32_t>(tk.m0 + rank * Cfg::BM);
+        const int32_t n0 = static_cast<int32_t>(tk.n0 + rank * (tk.bn / 2));
         for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty_i8[stage]), phase ^ 1u)) {
                 ok = false;
@@ -212,7 +223,9 @@ __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, cons
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 mbar_arrive_expect_tx(fb, Cfg::I8_STAGE_BYTES);
                 tma_load_2d(sa, tA, fb, k0, m0);
-                tma_load_2d(sa + Cfg::I8_A_BYTES, tB, fb, n0, k0);
+#pragma unroll
+                for (int a = 0; a < Cfg::I8_B_ATOMS; ++a)
+                    tma_load_2d(sa + Cfg::I8_A_BYTES + a * 8192, tB, fb, n0 + 128 * a, k0);
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -266,16 +279,34 @@ template <class Cfg>
 __device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
                           const Waiter &w)
 {
-    const int ct = threadIdx.x - 32 * Cfg::PRODUCER_WARPS;  // 0 .. CONV_THREADS-1
-    constexpr int A_PIECES = Cfg::BM * (Cfg::BK / 16);       // 16 int8 per piece
-    constexpr int B_ROW_PIECES = Cfg::BN / 16;
+    // CONV_GROUPS independent groups take alternate k-blocks (group g takes
+    // the k-blocks whose running index is g modulo the group count), so
+    // several k-blocks are widened at once and the latency of one group's
+    // load / widen / store / fence / signal chain is hidden.
+    constexpr int G = Cfg::CONV_GROUPS;
+    constexpr int GT = Cfg::CONV_THREADS / G;  // threads per group
+    const int ct = threadIdx.x - 32 * Cfg::PRODUCER_WARPS;
+    const int g = ct / GT, gt = ct % GT;
+    constexpr int A_PIECES = Cfg::BM * (Cfg::BK / 16);  // 16 int8 per piece
+    constexpr int B_ROW_PIECES = Cfg::CTA_BN / 16;
     constexpr int B_PIECES = Cfg::BK * B_ROW_PIECES;
-    static_assert(A_PIECES % Cfg::CONV_THREADS == 0 && B_PIECES % Cfg::CONV_THREADS == 0, "even split");
-    int si = 0, sf = 0;
-    uint32_t phi = 0, phf = 0;
+    constexpr int PIECES = A_PIECES + B_PIECES;
+    static_assert(A_PIECES % GT == 0 && B_PIECES % GT == 0, "even split");
+    constexpr int PER = PIECES / GT;  // pieces per thread per k-block
+    constexpr int BATCH = (A_PIECES / GT) < 8 ? (A_PIECES / GT) : 8;
+    static_assert((A_PIECES / GT) % BATCH == 0 && (B_PIECES / GT) % BATCH == 0, "batches do not straddle A and B");
+    // In a CTA pair the fp16 stage is complete when both CTAs have signalled
+    // the leader's full barrier.
+    const bool to_leader = Cfg::PAIR;
+    int64_t kcount = 0;
     for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
-        const int bn = task_of<Cfg>(p, u).bn;
-        for (int64_t kb = 0; kb < p.num_kb; ++kb) {
+        const int bn = Cfg::PAIR ? task_of<Cfg>(p, u).bn / 2 : task_of<Cfg>(p, u).bn;  // this CTA's columns
+        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kcount) {
+            if (kcount % G != g) continue;
+            const int si = static_cast<int>(kcount % Cfg::I8_STAGES);
+            const uint32_t phi = static_cast<uint32_t>((kcount / Cfg::I8_STAGES) & 1);
+            const int sf = static_cast<int>(kcount % Cfg::STAGES);
+            const uint32_t phf = static_cast<uint32_t>((kcount / Cfg::STAGES) & 1);
             bool got = w.wait(smem_u32(&ctl->full_i8[si]), phi);
             got = got && w.wait(smem_u32(&ctl->empty[sf]), phf ^ 1u);
             if (!__all_sync(0xffffffffu, got)) return;
@@ -283,47 +314,55 @@ __device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, 
             const uint32_t ib = ia + Cfg::I8_A_BYTES;
             const uint32_t fa = sbase + sf * Cfg::STAGE_BYTES;
             const uint32_t fb = fa + Cfg::A_BYTES;
-            constexpr int NA = A_PIECES / Cfg::CONV_THREADS, NB = B_PIECES / Cfg::CONV_THREADS;
-            // All shared loads of the k-block first (they pipeline), then the
-            // widening and the stores.
-            uint4 va[NA], vb[NB];
+#pragma unroll 1
+            for (int b0 = 0; b0 < PER; b0 += BATCH) {
+                // Shared loads of the batch first (they pipeline), then the
+                // widening and the stores.
+                uint4 v[BATCH];
+                const bool isA = b0 < A_PIECES / GT;
 #pragma unroll
-            for (int i = 0; i < NA; ++i) {
-                const int pc = ct + i * Cfg::CONV_THREADS;
-                va[i] = ld_shared_v4(ia + (pc >> 2) * 64 + (pc & 3) * 16);
-            }
+                for (int i = 0; i < BATCH; ++i) {
+                    if (isA) {
+                        const int pc = gt + (b0 + i) * GT;
+                        v[i] = ld_shared_v4(ia + (pc >> 2) * 64 + (pc & 3) * 16);
+                    } else {
+                        // B pieces run k-row fastest: eight lanes take eight
+                        // consecutive k rows of one 16-column piece, which the
+                        // 128-byte swizzle (int8 atoms on load, fp16 atoms on
+                        // store) spreads over all banks.
+                        const int pc = gt + (b0 + i - A_PIECES / GT) * GT;
+                        const int kk = pc % Cfg::BK, jn = pc / Cfg::BK;
+                        v[i] = ld_shared_v4(ib + (jn >> 3) * 8192 + kk * 128 + (((jn & 7) ^ (kk & 7)) << 4));
+                    }
+                }
 #pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                const int pc = ct + i * Cfg::CONV_THREADS;
-                vb[i] = ld_shared_v4(ib + (pc / B_ROW_PIECES) * Cfg::BN + (pc % B_ROW_PIECES) * 16);
-            }
-#pragma unroll
-            for (int i = 0; i < NA; ++i) {
-                const int pc = ct + i * Cfg::CONV_THREADS;
-                const int r = pc >> 2, j = pc & 3;  // row, 16-k piece of the 64-k row
-                const uint32_t row = fa + r * 128;
-                widen16_store(va[i], row + (((2 * j) ^ (r & 7)) << 4), row + (((2 * j + 1) ^ (r & 7)) << 4));
-            }
-#pragma unroll
-            for (int i = 0; i < NB; ++i) {
-                const int pc = ct + i * Cfg::CONV_THREADS;
-                const int kk = pc / B_ROW_PIECES, jn = pc % B_ROW_PIECES;  // k row, 16-n piece
-                if (jn * 16 < bn) {
-                    const uint32_t row = fb + (jn >> 2) * 8192 + kk * 128;
-                    const int c0 = (jn & 3) * 2;
-                    widen16_store(vb[i], row + ((c0 ^ (kk & 7)) << 4), row + (((c0 + 1) ^ (kk & 7)) << 4));
+                for (int i = 0; i < BATCH; ++i) {
+                    if (isA) {
+                        const int pc = gt + (b0 + i) * GT;
+                        const int r = pc >> 2, j = pc & 3;  // row, 16-k piece of the 64-k row
+                        const uint32_t row = fa + r * 128;
+                        widen16_store(v[i], row + (((2 * j) ^ (r & 7)) << 4), row + (((2 * j + 1) ^ (r & 7)) << 4));
+                    } else {
+                        const int pc = gt + (b0 + i - A_PIECES / GT) * GT;
+                        const int kk = pc % Cfg::BK, jn = pc / Cfg::BK;  // k row, 16-n piece
+                        if (jn * 16 < bn) {
+                            const uint32_t row = fb + (jn >> 2) * 8192 + kk * 128;
+                            const int c0 = (jn & 3) * 2;
+                            widen16_store(v[i], row + ((c0 ^ (kk & 7)) << 4), row + (((c0 + 1) ^ (kk & 7)) << 4));
+                        }
+                    }
                 }
             }
+            // Every store of the group reaches the async proxy, then one
+            // thread signals the stage (and frees the int8 slot).
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&ctl->full[sf]));
-            mbar_arrive(smem_u32(&ctl->empty_i8[si]));
-            if (++si == Cfg::I8_STAGES) {
-                si = 0;
-                phi ^= 1u;
-            }
-            if (++sf == Cfg::STAGES) {
-                sf = 0;
-                phf ^= 1u;
+            named_barrier_sync(1 + g, GT);
+            if (gt == 0) {
+                if (to_leader)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->full[sf]), 0));
+                else
+                    mbar_arrive(smem_u32(&ctl->full[sf]));
+                mbar_arrive(smem_u32(&ctl->empty_i8[si]));
             }
         }
     }
@@ -699,7 +738,36 @@ __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, c
                      r[4 * c + 3]);
     __syncwarp();
     uint32_t *C = static_cast<uint32_t *>(p.C);
-    if (p.vec_store) {
+    if (ADD && p.vec_store) {
+        // Read all eight 16-byte pieces of C first, then add and store, so
+        // the reads are in flight together.
+        uint4 old[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3), c = lane & 7;
+            const int64_t grow = row0 + rr, gcol = col0 + 4 * c;
+            old[it] = make_uint4(0, 0, 0, 0);
+            if (grow < p.M && gcol + 4 <= p.N)
+                old[it] = *reinterpret_cast<const uint4 *>(C + grow * p.ldc + gcol);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3), c = lane & 7;
+            const uint4 v = ld_shared_v4(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+            const int64_t grow = row0 + rr, gcol = col0 + 4 * c;
+            if (grow < p.M && gcol < p.N) {
+                uint32_t *dst = C + grow * p.ldc + gcol;
+                if (gcol + 4 <= p.N) {
+                    const uint4 o = old[it];
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+                } else {
+                    dst[0] += v.x;
+                    if (gcol + 1 < p.N) dst[1] += v.y;
+                    if (gcol + 2 < p.N) dst[2] += v.z;
+                }
+            }
+        }
+    } else if (p.vec_store) {
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
             const int rr = it * 4 + (lane >> 3), c = lane & 7;
@@ -746,8 +814,8 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
         const int ncols = tk.bn / 2;  // this warp's columns
         const int64_t row0 = tk.m0 + rank * Cfg::BM + q * 32;
         const int64_t colb = tk.n0 + h * ncols;
-        uint32_t isum[(Cfg::INT_OUT && !Cfg::CONVERT) ? Cfg::EPI_COLS : 1];
-        if constexpr (Cfg::INT_OUT && !Cfg::CONVERT) {
+        uint32_t isum[(Cfg::INT_OUT && !Cfg::SUM_IN_C) ? Cfg::EPI_COLS : 1];
+        if constexpr (Cfg::INT_OUT && !Cfg::SUM_IN_C) {
 #pragma unroll
             for (int i = 0; i < Cfg::EPI_COLS; ++i) isum[i] = 0;
         }
@@ -756,7 +824,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             if (!__all_sync(0xffffffffu, got)) return;
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * ncols;
-            if constexpr (Cfg::CONVERT) {
+            if constexpr (Cfg::SUM_IN_C) {
                 // Chunk partials are exact integers; the first chunk stores
                 // them, later chunks add into C (each element is read and
                 // written by the same thread, in chunk order).
@@ -812,7 +880,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if constexpr (Cfg::INT_OUT && !Cfg::CONVERT) {
+        if constexpr (Cfg::INT_OUT && !Cfg::SUM_IN_C) {
 #pragma unroll
             for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb)
                 if (jb < ncols / 32) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
@@ -838,12 +906,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]),
-                      Cfg::LDG ? Cfg::PRODUCER_THREADS : (Cfg::CONVERT ? Cfg::CONV_THREADS : 1));
+                      Cfg::LDG ? Cfg::PRODUCER_THREADS : (Cfg::CONVERT ? (Cfg::PAIR ? 2 : 1) : 1));
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int s = 0; s < Cfg::I8_STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full_i8[s]), 1);
-            mbar_init(smem_u32(&ctl->empty_i8[s]), Cfg::CONV_THREADS);
+            mbar_init(smem_u32(&ctl->empty_i8[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -880,7 +948,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if constexpr (Cfg::LDG) {
             producer_ldg<Cfg>(p, sbase, ctl, w);
         } else if constexpr (Cfg::CONVERT) {
-            if (lane == 0) producer_tma_i8<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
+            if (lane == 0) producer_tma_i8<Cfg>(p, &tmA, &tmB, sbase, ctl, w);  // single CTA or pair
         } else if constexpr (Cfg::PAIR) {
             if (lane == 0) producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
         } else {

@@ -9,6 +9,7 @@ static const Variant kS8Variants[] = {
     make_variant<GemmCfg<128, 6, false, true>>(),
     make_variant<GemmCfg<256, 2, false, true, true, 4>>(),  // int8 TMA + in-kernel widening
     make_variant<GemmCfg<128, 3, false, true, true, 6>>(),
+    make_variant<GemmCfg<256, 4, false, true, true, 4, true, 1, 2>>(),  // CTA pair + in-kernel widening (opt-in)
 };
 
 int variants_s8(const Variant **out)

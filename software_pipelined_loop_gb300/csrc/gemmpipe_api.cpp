@@ -148,8 +148,10 @@ const Variant *find_variant(int int_out, int convert, int producer, int bn, int 
 // TMA needs 16-byte aligned bases and row pitches (K and N multiples of 16
 // int8).  It is taken only when asked for (producer override 0): widening
 // inside the kernel redoes the conversion of every operand tile for every
-// output tile that reads it, which costs more shared-memory bandwidth than
-// one widening pass over the operands.
+// output tile that reads it through the load/store pipe while the tensor
+// cores read shared memory, and in a CTA pair each k-block needs a
+// cross-CTA release-arrive from the peer's converters; measured, both make
+// it slower than one widening pass plus the fp16 kernel.
 bool s8_convert_ok(const void *A, int64_t K, const void *B, int64_t N)
 {
     if (!(aligned16(A) && aligned16(B) && K % 16 == 0 && N % 16 == 0)) return false;
@@ -179,8 +181,8 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // A CTA pair (256 x 256 tiles, cta_group::2 MMA) when both dimensions
     // exceed one 128-row / 128-column tile and TMA reads the operands.
     const Variant *v = nullptr;
-    if (producer == 0 && !convert && bn == 256 && M > kBM && N > 128) {
-        v = find_variant(int_out, 0, 0, 256, ov.stages, 1);
+    if (producer == 0 && bn == 256 && M > kBM && N > 128) {
+        v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;
     }
     if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages, 0);
@@ -239,7 +241,7 @@ EncodeFn encode_fn()
 // outside it.  fp16: 128-byte swizzle, box 64 columns x box_rows rows.
 // int8: no swizzle, box box_cols x box_rows.
 bool encode_2d_any(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
-                   int box_rows, bool int8)
+                   int box_rows, bool int8, bool swizzle128 = false)
 {
     EncodeFn f = encode_fn();
     if (!f) return false;
@@ -250,7 +252,8 @@ bool encode_2d_any(CUtensorMap *m, const void *base, int64_t rows, int64_t cols,
     const cuuint32_t estr[2] = {1, 1};
     return f(m, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base),
              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             (int8 && !swizzle128) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -343,8 +346,10 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (pl.v->info.convert) {
+        // int8: A box 64 (k) x 128 rows unswizzled; B in 128 x 64 atoms with
+        // the 128-byte swizzle.
         if (!encode_2d_any(&ta, A, M, K, lda, kBK, kBM, true) ||
-            !encode_2d_any(&tb, B, K, N, ldb, pl.v->info.BN, kBK, true))
+            !encode_2d_any(&tb, B, K, N, ldb, 128, kBK, true, true))
             return GEMMPIPE_ERR_INTERNAL;
     } else if (pl.v->info.producer == 0) {
         // Boxes: A 64 (k) x 128 rows, B 64 (n) x 64 (k); a pair CTA loads the
