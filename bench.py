@@ -5,8 +5,10 @@
 Headline (``value``): INT8 IGEMM M = N = K = 4096 (the pages' benchmark shape),
 int8 operands uniform on [-128, 127], int32 C, in TOPS.  A step is one
 gemm_s8s8s32 call through the C ABI with inputs resident in HBM.  Because the
-inputs (32 MiB) fit in the 126 MiB L2, a 256 MiB buffer is written between
-timed steps and each step is timed alone with CUDA events on its stream.
+inputs (32 MiB) fit in the 126 MiB L2, a 256 MiB buffer is written and
+another 256 MiB read between timed steps (no input cached, no dirty lines
+left for the timed step to write back), and each step is timed alone with
+CUDA events on its stream.
 
 Also measured in the same run and reported under ``secondary``: FP16
 4096^3 (TFLOPS), the skinny FP16 16384 x 128 x 16384 (GB/s of algorithmic
@@ -330,8 +332,17 @@ def run_gpu(args) -> int:
         dist.barrier()
     gemmpipe.load()
     peaks, peak_src = load_peaks()
+    # L2 flush between timed steps: write a buffer larger than L2, then read
+    # another one, so the timed step starts with none of its data cached and
+    # with clean lines (the write-back of the flush's own dirty lines is not
+    # charged to the timed step).
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush = lambda: flush_buf.zero_()
+    clean_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+        torch.sum(clean_buf, dim=0, dtype=torch.int64, out=flush_sink)
 
     clock = ClockSampler(local)
     clock.start()
@@ -391,7 +402,8 @@ def run_gpu(args) -> int:
                       "fp16 operands, tcgen05 kind::f16, fp32 accumulation and output",
         "data": "synthetic",
         "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
-                   "l2": head["l2"] + " (256 MiB buffer written between timed steps when inputs < L2)",
+                   "l2": head["l2"] + " (between timed steps: 256 MiB written, then another 256 MiB read, "
+                                      "when inputs < L2)",
                    "plan": {k: head["plan"][k] for k in ("producer", "BN", "stages", "threads", "grid", "tasks",
                                                          "operand_copy")},
                    "replicas": world},
@@ -416,6 +428,76 @@ def fp16_4096():
     return ("fp16_4096", "f16", 4096, 4096, 4096, A, B)
 
 
+ABLATION = [
+    # (label, dtype, producer, bn, stages, cta_pair)
+    ("pair S=1 (load, wait, compute)", "f16", 0, 256, 1, 1),
+    ("pair S=2 (double buffer)", "f16", 0, 256, 2, 1),
+    ("pair S=4", "f16", 0, 256, 4, 1),
+    ("pair S=6 (default)", "f16", 0, 256, 6, 1),
+    ("single CTA 128x256 S=4", "f16", 0, 256, 4, 0),
+    ("single CTA 128x128 S=6", "f16", 0, 128, 6, 0),
+    ("single CTA bounded-load producer 128x256 S=4", "f16", 1, 256, 4, 0),
+    ("int8: widening pass + pair (default)", "s8", -1, 0, 0, -1),
+    ("int8: in-kernel widening, pair", "s8", 0, 256, 4, 1),
+    ("int8: in-kernel widening, single CTA", "s8", 0, 256, 2, 0),
+]
+
+
+def run_ablation(args) -> int:
+    """Ring depth and producer ablation at 4096^3 (one JSON line)."""
+    import torch
+
+    from software_pipelined_loop_gb300 import build, gemmpipe, inputs
+    build.build()
+    gemmpipe.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+        torch.sum(clean_buf, dim=0, dtype=torch.int64, out=sink)
+
+    M = N = K = 4096
+    ops = {}
+    rows = []
+    for label, dt, producer, bn, stages, pair in ABLATION:
+        if dt not in ops:
+            A, B = inputs.make_operands(dt, M, N, K, inputs.SEED_BASE + 5)
+            ops[dt] = (torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev),
+                       torch.empty((M, N), dtype=torch.int32 if dt == "s8" else torch.float32, device=dev))
+        Ad, Bd, C = ops[dt]
+        fn = gemmpipe.gemm_s8s8s32 if dt == "s8" else gemmpipe.gemm_f16f32
+        stream = torch.cuda.current_stream(dev)
+        gemmpipe.gemmpipe_set_plan_override(producer, bn, stages, pair)
+        try:
+            plan = gemmpipe.gemmpipe_plan(0 if dt == "s8" else 1, M, N, K, Ad, Bd, C)
+            call = lambda: fn(M, N, K, Ad, Bd, C, stream)
+            for _ in range(max(3, args.warmup)):
+                call()
+            torch.cuda.synchronize()
+            gemmpipe.gemmpipe_timing_read()
+            gemmpipe.gemmpipe_timing_enable(True)
+            times = time_steps(call, max(5, args.steps // 10), flush, stream)
+            gms, gn, ams, an = gemmpipe.gemmpipe_timing_read()
+            gemmpipe.gemmpipe_timing_enable(False)
+        finally:
+            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1)
+        st = gemmpipe.gemmpipe_get_device_status(stream)
+        ms = statistics.mean(times)
+        rows.append({"config": label, "ms_per_step": ms, "per_step": 2.0 * M * N * K / ms / 1e9,
+                     "kernel_ms": gms / max(1, gn), "status": st,
+                     "plan": {k: plan[k] for k in ("producer", "BM", "BN", "stages", "cta_pair", "operand_copy")}})
+    base = rows[0]["ms_per_step"]
+    for r in rows:
+        r["speedup_vs_S1"] = base / r["ms_per_step"] if r["plan"]["cta_pair"] else None
+    print(json.dumps({"ablation": "ring depth and producer, 4096^3", "unit": "TFLOPS or TOPS per step",
+                      "rows": rows}), flush=True)
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,7 +512,9 @@ def main() -> int:
                     help="time dtype,M,N,K (s8 or f16) as the headline instead of INT8 4096^3 "
                          "(for profiling and sweeps; uniform inputs)")
     ap.add_argument("--force", default=None,
-                    help="plan override producer,bn,stages (see gemmpipe_set_plan_override)")
+                    help="plan override producer,bn,stages[,cta_pair] (see gemmpipe_set_plan_override)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="ring-depth / producer ablation at 4096^3 instead of the benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -446,6 +530,8 @@ def main() -> int:
         gemmpipe.gemmpipe_set_plan_override(*[int(x) for x in args.force.split(",")])
     if args.impl == "reference":
         return run_reference(args)
+    if args.ablation:
+        return run_ablation(args)
     return run_gpu(args)
 
 

@@ -232,12 +232,12 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * in-kernel widening of int8 tiles), 1 bounded-load producer for
  * gemm_f16f32 and the workspace-widening path for gemm_s8s8s32.  bn: 0
  * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
- * depths (a depth only a single-CTA variant has, such as 4 for 256-wide
- * tiles, also selects single CTAs over CTA pairs; see gemmpipe_plan for what
- * was taken).  Returns INVALID_VALUE for
- * values outside these sets.
+ * ring depths (when the chosen variant has no such depth the automatic one
+ * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
+ * 0 single CTAs, 1 CTA pairs where the shape allows them.  Returns
+ * INVALID_VALUE for values outside these sets.
  */
-GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages);
+GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair);
 
 /* Frees every INT8 workspace (synchronizes the device first). */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_release_workspaces(void);

@@ -130,9 +130,10 @@ __device__ __forceinline__ void pad_piece(const PadJob &j, int64_t r, int64_t c)
 }
 
 // x covers 8-element pieces of a row, y strides over rows, two rows in
-// flight per thread.
-__global__ void pad_f16_kernel(const PadJob j)
+// flight per thread; z picks one of two jobs (A and B padded in one launch).
+__global__ void pad_f16_kernel(const PadJob j0, const PadJob j1)
 {
+    const PadJob &j = blockIdx.z == 0 ? j0 : j1;
     const int64_t c = 8 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
     if (c >= j.pitch) return;
     const int64_t step = gridDim.y;
@@ -192,17 +193,23 @@ cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, u
     return cudaGetLastError();
 }
 
-cudaError_t launch_pad_f16(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch, int sms,
-                           cudaStream_t s)
+cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
+                           const uint16_t *src1, int64_t rows1, int64_t cols1, uint16_t *dst1, int64_t pitch1,
+                           int sms, cudaStream_t s)
 {
-    const PadJob j{src, rows, cols, dst, pitch};
+    // rows1 == 0: one job only.
+    const PadJob j0{src0, rows0, cols0, dst0, pitch0};
+    const PadJob j1{src1, rows1, cols1, dst1, pitch1};
     const int threads = 128;
-    const int64_t gx = (pitch / 8 + threads - 1) / threads;
+    const int64_t maxpitch = pitch0 > pitch1 ? pitch0 : pitch1;
+    const int64_t maxrows = rows0 > rows1 ? rows0 : rows1;
+    const int64_t gx = (maxpitch / 8 + threads - 1) / threads;
     int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
-    gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
+    gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
     gy = gy > 65535 ? 65535 : gy;
     if (gx > 2147483647) return cudaErrorInvalidValue;
-    pad_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1), threads, 0, s>>>(j);
+    const unsigned gz = rows1 > 0 ? 2u : 1u;
+    pad_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), gz), threads, 0, s>>>(j0, j1);
     return cudaGetLastError();
 }
 

@@ -112,7 +112,7 @@ gemmpipe_status_t check_device_pointers(int64_t K, const void *A, const void *B,
 // ------------------------------------------------------------------ plans
 
 struct Override {
-    int producer = -1, bn = 0, stages = 0;
+    int producer = -1, bn = 0, stages = 0, pair = -1;
 };
 Override g_override;
 
@@ -181,7 +181,7 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // A CTA pair (256 x 256 tiles, cta_group::2 MMA) when both dimensions
     // exceed one 128-row / 128-column tile and TMA reads the operands.
     const Variant *v = nullptr;
-    if (producer == 0 && bn == 256 && M > kBM && N > 128) {
+    if (producer == 0 && bn == 256 && M > kBM && N > 128 && ov.pair != 0) {
         v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;
     }
@@ -420,11 +420,14 @@ bool pad_wanted(const void *A, int64_t K, const void *B, int64_t N)
     return g_override.producer != 1;
 }
 
-gemmpipe_status_t pad_operand(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch,
-                              const DeviceInfo &d, cudaStream_t s)
+// Pads one or two operands (rows1 == 0: one) in a single launch.
+gemmpipe_status_t pad_operands(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
+                               const uint16_t *src1, int64_t rows1, int64_t cols1, uint16_t *dst1, int64_t pitch1,
+                               const DeviceInfo &d, cudaStream_t s)
 {
     TimedRegion tr(false, s);
-    const cudaError_t e = gp::launch_pad_f16(src, rows, cols, dst, pitch, d.sms, s);
+    const cudaError_t e =
+        gp::launch_pad_f16(src0, rows0, cols0, dst0, pitch0, src1, rows1, cols1, dst1, pitch1, d.sms, s);
     tr.end();
     if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
@@ -529,15 +532,21 @@ gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_ha
         void *ws = nullptr;
         if (workspace(dev, s, bytes, &ws) == GEMMPIPE_OK) {
             uint16_t *w = static_cast<uint16_t *>(ws);
+            uint16_t *wa = pa ? w : nullptr;
+            uint16_t *wb = pb ? w + (pa ? M * Kp : 0) : nullptr;
+            if (pa && pb)
+                st = pad_operands(A, M, K, wa, Kp, B, K, N, wb, Np, d, s);
+            else if (pa)
+                st = pad_operands(A, M, K, wa, Kp, nullptr, 0, 0, nullptr, 0, d, s);
+            else
+                st = pad_operands(B, K, N, wb, Np, nullptr, 0, 0, nullptr, 0, d, s);
+            if (st != GEMMPIPE_OK) return st;
             if (pa) {
-                if ((st = pad_operand(A, M, K, w, Kp, d, s)) != GEMMPIPE_OK) return st;
-                Ause = w;
+                Ause = wa;
                 lda = Kp;
-                w += M * Kp;
             }
             if (pb) {
-                if ((st = pad_operand(B, K, N, w, Np, d, s)) != GEMMPIPE_OK) return st;
-                Buse = w;
+                Buse = wb;
                 ldb = Np;
             }
         }
@@ -690,15 +699,17 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     return GEMMPIPE_OK;
 }
 
-gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages)
+gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair)
 {
     if (producer < -1 || producer > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_override.producer = producer;
     g_override.bn = bn;
     g_override.stages = stages;
+    g_override.pair = cta_pair;
     return GEMMPIPE_OK;
 }
 

@@ -38,8 +38,9 @@ int variants_s8(const Variant **out);
 cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16, int64_t pitchA16,
                                 const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB16,
                                 int sms, cudaStream_t s);
-cudaError_t launch_pad_f16(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch, int sms,
-                           cudaStream_t s);
+cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
+                           const uint16_t *src1, int64_t rows1, int64_t cols1, uint16_t *dst1, int64_t pitch1,
+                           int sms, cudaStream_t s);
 cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t status_word(int **ptr);  // device address of the current device's status word

@@ -391,7 +391,7 @@ def test_cta_pair_matches_single_cta(dev, dtype, M, N, K):
     plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
     assert plan["cta_pair"] == 1 and plan["BM"] == 256
     check(run(A, B, dev))
-    gemmpipe.gemmpipe_set_plan_override(-1, 256, 4)
+    gemmpipe.gemmpipe_set_plan_override(-1, 256, 0, 0)
     try:
         plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
         assert plan["cta_pair"] == 0 and plan["BM"] == 128
@@ -461,3 +461,21 @@ def test_s8_stall_times_out_in_converter_variant(dev):
     finally:
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert np.array_equal(C.cpu().numpy(), oracle.gemm_s8s8s32(A, B))
+
+
+@pytest.mark.parametrize("stages", [1, 2, 4, 6])
+def test_ring_depths_of_cta_pair(dev, stages):
+    # S = 1: the producer waits for the MMAs to release the only stage
+    # before every load (load, wait, compute -- no overlap); S = 2: the
+    # double buffer; deeper rings overlap more k-blocks.  Results must not
+    # depend on the depth.
+    M, N, K = 520, 776, 1000
+    A, B = inputs.make_operands("f16", M, N, K, seed=800 + stages)
+    gemmpipe.gemmpipe_set_plan_override(0, 256, stages, 1)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert plan["stages"] == stages and plan["cta_pair"] == 1
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert_f16_close(got, oracle.gemm_f16f32(A, B), f"S={stages}")
