@@ -312,6 +312,22 @@ def measure_e2e(res: dict, steps: int, dev) -> dict:
             "d2h_bytes_per_step": Ch.numel() * Ch.element_size()}
 
 
+def slowest_rank_ms(ms: float, dist=None, device=None) -> float:
+    """Max over ranks of a per-step time (the job's step time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ops_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job throughput in T(FL)OPS: every rank's operations over the
+    slowest rank's step time (replicas: one copy of the workload per rank)."""
+    return world * ops_per_rank / ms / 1e9
+
+
 def run_gpu(args) -> int:
     import torch
 
@@ -366,12 +382,8 @@ def run_gpu(args) -> int:
     finally:
         clock.stop()
 
-    ms = head["ms"]
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * head["flops"] / ms / 1e9
+    ms = slowest_rank_ms(head["ms"], dist, dev)
+    value = job_throughput(head["flops"], ms, world)
     unit = "TOPS" if head["dtype"] == "s8" else "TFLOPS"
     if rank != 0:
         if dist:

@@ -35,36 +35,38 @@ struct WidenJob {
     int64_t pitch;  // destination row pitch in elements, a multiple of 8
 };
 
-// One 16-element piece of one row: loads the source bytes (one 16-byte load
-// when the row is 16-byte aligned and the piece is whole, else byte loads),
-// writes 16 fp16 values (the slots past `cols` as zero).
-__device__ __forceinline__ void widen_piece(const WidenJob &j, int64_t r, int64_t c)
+// Loads the 16 int8 of one piece of row r (one 16-byte load when the row
+// is 16-byte aligned and the piece whole, else byte loads of the valid ones).
+__device__ __forceinline__ uint4 widen_load(const WidenJob &j, int64_t r, int64_t c)
 {
     const int8_t *src = j.src + r * j.cols + c;
     const int64_t valid = j.cols - c;
+    if (valid >= 16 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
+        return __ldg(reinterpret_cast<const uint4 *>(src));
     uint32_t w[4];
-    if (valid >= 16 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
-    } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t x = 0;
+    for (int q = 0; q < 4; ++q) {
+        uint32_t x = 0;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (4 * q + b < valid) x |= static_cast<uint32_t>(static_cast<uint8_t>(src[4 * q + b])) << (8 * b);
-            w[q] = x;
-        }
+        for (int b = 0; b < 4; ++b)
+            if (4 * q + b < valid) x |= static_cast<uint32_t>(static_cast<uint8_t>(src[4 * q + b])) << (8 * b);
+        w[q] = x;
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Widens a loaded piece and writes its 16 fp16 values (slots past `cols` as
+// zero: their bytes were loaded as 0, which widens to 0, and the mask keeps
+// that independent of the load path).
+__device__ __forceinline__ void widen_store(const WidenJob &j, int64_t r, int64_t c, const uint4 &v)
+{
     uint32_t o[8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) widen4(w[q], o[2 * q], o[2 * q + 1]);
+    widen4(v.x, o[0], o[1]);
+    widen4(v.y, o[2], o[3]);
+    widen4(v.z, o[4], o[5]);
+    widen4(v.w, o[6], o[7]);
+    const int64_t valid = j.cols - c;
     if (valid < 16) {
-        // Bytes past the row were read as 0 and widen to 0 already; the mask
-        // keeps the zero padding independent of that.
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int64_t e = 2 * q;
@@ -78,7 +80,8 @@ __device__ __forceinline__ void widen_piece(const WidenJob &j, int64_t r, int64_
 }
 
 // blockIdx.z picks the matrix (0: A, 1: B); x covers 16-element pieces of a
-// row, y strides over rows, two rows in flight per thread.
+// row, y strides over rows.  Four rows' loads are issued before any of them
+// is widened and stored, so each thread keeps four loads in flight.
 __global__ void widen_s8_f16_kernel(const WidenJob ja, const WidenJob jb)
 {
     const WidenJob &j = blockIdx.z == 0 ? ja : jb;
@@ -86,11 +89,17 @@ __global__ void widen_s8_f16_kernel(const WidenJob ja, const WidenJob jb)
     if (c >= j.pitch) return;
     const int64_t step = gridDim.y;
     int64_t r = blockIdx.y;
-    for (; r + step < j.rows; r += 2 * step) {
-        widen_piece(j, r, c);
-        widen_piece(j, r + step, c);
+    for (; r + 3 * step < j.rows; r += 4 * step) {
+        const uint4 v0 = widen_load(j, r, c);
+        const uint4 v1 = widen_load(j, r + step, c);
+        const uint4 v2 = widen_load(j, r + 2 * step, c);
+        const uint4 v3 = widen_load(j, r + 3 * step, c);
+        widen_store(j, r, c, v0);
+        widen_store(j, r + step, c, v1);
+        widen_store(j, r + 2 * step, c, v2);
+        widen_store(j, r + 3 * step, c, v3);
     }
-    if (r < j.rows) widen_piece(j, r, c);
+    for (; r < j.rows; r += step) widen_store(j, r, c, widen_load(j, r, c));
 }
 
 // Copies a rows x cols fp16 matrix (densely packed, any 2-byte alignment)
@@ -106,18 +115,30 @@ struct PadJob {
     int64_t pitch;
 };
 
-__device__ __forceinline__ void pad_piece(const PadJob &j, int64_t r, int64_t c)
+struct PadLoad {
+    uint4 w0, w1;
+    uint32_t s;
+};
+
+__device__ __forceinline__ PadLoad pad_load(const PadJob &j, int64_t r, int64_t c)
 {
     const uintptr_t lo = reinterpret_cast<uintptr_t>(j.src + r * j.cols);
     const uintptr_t hi = lo + 2 * static_cast<uintptr_t>(j.cols);
     const uintptr_t a = lo + 2 * static_cast<uintptr_t>(c);
-    const uint32_t s = static_cast<uint32_t>(a & 15u);
-    const uintptr_t base = a - s;
-    uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
-    if (base < hi && base + 16 > lo) w0 = __ldg(reinterpret_cast<const uint4 *>(base));
-    if (s != 0 && base + 16 < hi) w1 = __ldg(reinterpret_cast<const uint4 *>(base + 16));
+    PadLoad L;
+    L.s = static_cast<uint32_t>(a & 15u);
+    const uintptr_t base = a - L.s;
+    L.w0 = make_uint4(0, 0, 0, 0);
+    L.w1 = make_uint4(0, 0, 0, 0);
+    if (base < hi && base + 16 > lo) L.w0 = __ldg(reinterpret_cast<const uint4 *>(base));
+    if (L.s != 0 && base + 16 < hi) L.w1 = __ldg(reinterpret_cast<const uint4 *>(base + 16));
+    return L;
+}
+
+__device__ __forceinline__ void pad_store(const PadJob &j, int64_t r, int64_t c, const PadLoad &L)
+{
     uint32_t o[4];
-    realign16(w0, w1, s, o);
+    realign16(L.w0, L.w1, L.s, o);
     const int64_t valid = j.cols - c;
     if (valid < 8) {
 #pragma unroll
@@ -129,8 +150,9 @@ __device__ __forceinline__ void pad_piece(const PadJob &j, int64_t r, int64_t c)
     *reinterpret_cast<uint4 *>(j.dst + r * j.pitch + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// x covers 8-element pieces of a row, y strides over rows, two rows in
-// flight per thread; z picks one of two jobs (A and B padded in one launch).
+// x covers 8-element pieces of a row, y strides over rows with four rows'
+// loads in flight per thread; z picks one of two jobs (A and B padded in
+// one launch).
 __global__ void pad_f16_kernel(const PadJob j0, const PadJob j1)
 {
     const PadJob &j = blockIdx.z == 0 ? j0 : j1;
@@ -138,11 +160,17 @@ __global__ void pad_f16_kernel(const PadJob j0, const PadJob j1)
     if (c >= j.pitch) return;
     const int64_t step = gridDim.y;
     int64_t r = blockIdx.y;
-    for (; r + step < j.rows; r += 2 * step) {
-        pad_piece(j, r, c);
-        pad_piece(j, r + step, c);
+    for (; r + 3 * step < j.rows; r += 4 * step) {
+        const PadLoad l0 = pad_load(j, r, c);
+        const PadLoad l1 = pad_load(j, r + step, c);
+        const PadLoad l2 = pad_load(j, r + 2 * step, c);
+        const PadLoad l3 = pad_load(j, r + 3 * step, c);
+        pad_store(j, r, c, l0);
+        pad_store(j, r + step, c, l1);
+        pad_store(j, r + 2 * step, c, l2);
+        pad_store(j, r + 3 * step, c, l3);
     }
-    if (r < j.rows) pad_piece(j, r, c);
+    for (; r < j.rows; r += step) pad_store(j, r, c, pad_load(j, r, c));
 }
 
 __global__ void zero_fill_kernel(uint8_t *dst, int64_t bytes)
@@ -186,6 +214,8 @@ cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, u
     const int64_t maxrows = rowsA > rowsB ? rowsA : rowsB;
     // About eight blocks of 128 threads per SM for each matrix.
     int64_t gy = (static_cast<int64_t>(sms) * 8 + gx - 1) / gx;
+    // Prefer whole groups of four rows per y-block.
+    if (gy * 4 > maxrows) gy = (maxrows + 3) / 4;
     gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
     gy = gy > 65535 ? 65535 : gy;
     if (gx > 2147483647) return cudaErrorInvalidValue;
@@ -205,6 +235,7 @@ cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, u
     const int64_t maxrows = rows0 > rows1 ? rows0 : rows1;
     const int64_t gx = (maxpitch / 8 + threads - 1) / threads;
     int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
+    if (gy * 4 > maxrows) gy = (maxrows + 3) / 4;
     gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
     gy = gy > 65535 ? 65535 : gy;
     if (gx > 2147483647) return cudaErrorInvalidValue;
