@@ -402,7 +402,7 @@ def run_gpu(args) -> int:
         val = r["bytes_per_s"] if r["N"] <= 128 else r["ops_per_s"]
         return {"value": val, "unit": unit, "ms_per_step": r["ms"], "kernel_ms": r["kernel_ms"],
                 "roofline": r["roofline"], "l2": r["l2"],
-                "plan": {k: r["plan"][k] for k in ("producer", "BN", "stages", "grid", "tiles")},
+                "plan": {k: r["plan"][k] for k in ("producer", "BN", "stages", "grid", "tiles", "split_tiles")},
                 "shape": [r["M"], r["N"], r["K"]]}
 
     line = {
@@ -416,7 +416,7 @@ def run_gpu(args) -> int:
         "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
                    "l2": head["l2"] + " (between timed steps: 256 MiB written, then another 256 MiB read, "
                                       "when inputs < L2)",
-                   "plan": {k: head["plan"][k] for k in ("producer", "BN", "stages", "threads", "grid", "tasks",
+                   "plan": {k: head["plan"][k] for k in ("producer", "BN", "stages", "threads", "grid", "units", "split_tiles",
                                                          "operand_copy")},
                    "replicas": world},
         "roofline": head["roofline"],
@@ -440,23 +440,32 @@ def fp16_4096():
     return ("fp16_4096", "f16", 4096, 4096, 4096, A, B)
 
 
+SQUARE = (4096, 4096, 4096)
+RAGGED = (4093, 3001, 4107)
+SKINNY = (16384, 128, 16384)
 ABLATION = [
-    # (label, dtype, producer, bn, stages, cta_pair)
-    ("pair S=1 (load, wait, compute)", "f16", 0, 256, 1, 1),
-    ("pair S=2 (double buffer)", "f16", 0, 256, 2, 1),
-    ("pair S=4", "f16", 0, 256, 4, 1),
-    ("pair S=6 (default)", "f16", 0, 256, 6, 1),
-    ("single CTA 128x256 S=4", "f16", 0, 256, 4, 0),
-    ("single CTA 128x128 S=6", "f16", 0, 128, 6, 0),
-    ("single CTA bounded-load producer 128x256 S=4", "f16", 1, 256, 4, 0),
-    ("int8: widening pass + pair (default)", "s8", -1, 0, 0, -1),
-    ("int8: in-kernel widening, pair", "s8", 0, 256, 4, 1),
-    ("int8: in-kernel widening, single CTA", "s8", 0, 256, 2, 0),
+    # (label, dtype, shape, producer, bn, stages, cta_pair, split)
+    ("pair S=1 (load, wait, compute)", "f16", SQUARE, 0, 256, 1, 1, -1),
+    ("pair S=2 (double buffer)", "f16", SQUARE, 0, 256, 2, 1, -1),
+    ("pair S=4", "f16", SQUARE, 0, 256, 4, 1, -1),
+    ("pair S=6 (default)", "f16", SQUARE, 0, 256, 6, 1, -1),
+    ("pair S=6, every tile whole (no stream-K)", "f16", SQUARE, 0, 256, 6, 1, 0),
+    ("single CTA 128x256 S=4", "f16", SQUARE, 0, 256, 4, 0, -1),
+    ("single CTA 128x128 S=6", "f16", SQUARE, 0, 128, 6, 0, -1),
+    ("single CTA bounded-load producer 128x256 S=4", "f16", SQUARE, 1, 256, 4, 0, -1),
+    ("int8: widening pass + pair (default)", "s8", SQUARE, -1, 0, 0, -1, -1),
+    ("int8: widening pass + pair, every tile whole", "s8", SQUARE, -1, 0, 0, -1, 0),
+    ("int8: in-kernel widening, pair", "s8", SQUARE, 0, 256, 4, 1, -1),
+    ("int8: in-kernel widening, single CTA", "s8", SQUARE, 0, 256, 2, 0, -1),
+    ("ragged fp16: stream-K (default)", "f16", RAGGED, -1, 0, 0, -1, -1),
+    ("ragged fp16: every tile whole", "f16", RAGGED, -1, 0, 0, -1, 0),
+    ("skinny fp16: stream-K (default)", "f16", SKINNY, -1, 0, 0, -1, -1),
+    ("skinny fp16: every tile whole", "f16", SKINNY, -1, 0, 0, -1, 0),
 ]
 
 
 def run_ablation(args) -> int:
-    """Ring depth and producer ablation at 4096^3 (one JSON line)."""
+    """Ring depth, producer and stream-K ablation (one JSON line)."""
     import torch
 
     from software_pipelined_loop_gb300 import build, gemmpipe, inputs
@@ -472,18 +481,19 @@ def run_ablation(args) -> int:
         flush_buf.zero_()
         torch.sum(clean_buf, dim=0, dtype=torch.int64, out=sink)
 
-    M = N = K = 4096
     ops = {}
     rows = []
-    for label, dt, producer, bn, stages, pair in ABLATION:
-        if dt not in ops:
+    for label, dt, shape, producer, bn, stages, pair, split in ABLATION:
+        M, N, K = shape
+        if (dt, shape) not in ops:
             A, B = inputs.make_operands(dt, M, N, K, inputs.SEED_BASE + 5)
-            ops[dt] = (torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev),
-                       torch.empty((M, N), dtype=torch.int32 if dt == "s8" else torch.float32, device=dev))
-        Ad, Bd, C = ops[dt]
+            ops[(dt, shape)] = (torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev),
+                                torch.empty((M, N), dtype=torch.int32 if dt == "s8" else torch.float32,
+                                            device=dev))
+        Ad, Bd, C = ops[(dt, shape)]
         fn = gemmpipe.gemm_s8s8s32 if dt == "s8" else gemmpipe.gemm_f16f32
         stream = torch.cuda.current_stream(dev)
-        gemmpipe.gemmpipe_set_plan_override(producer, bn, stages, pair)
+        gemmpipe.gemmpipe_set_plan_override(producer, bn, stages, pair, split)
         try:
             plan = gemmpipe.gemmpipe_plan(0 if dt == "s8" else 1, M, N, K, Ad, Bd, C)
             call = lambda: fn(M, N, K, Ad, Bd, C, stream)
@@ -496,16 +506,20 @@ def run_ablation(args) -> int:
             gms, gn, ams, an = gemmpipe.gemmpipe_timing_read()
             gemmpipe.gemmpipe_timing_enable(False)
         finally:
-            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1)
+            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
         st = gemmpipe.gemmpipe_get_device_status(stream)
         ms = statistics.mean(times)
-        rows.append({"config": label, "ms_per_step": ms, "per_step": 2.0 * M * N * K / ms / 1e9,
-                     "kernel_ms": gms / max(1, gn), "status": st,
-                     "plan": {k: plan[k] for k in ("producer", "BM", "BN", "stages", "cta_pair", "operand_copy")}})
+        kms = gms / max(1, gn)
+        rows.append({"config": label, "shape": list(shape), "ms_per_step": ms,
+                     "per_step": 2.0 * M * N * K / ms / 1e9, "kernel_ms": kms,
+                     "per_kernel": 2.0 * M * N * K / kms / 1e9, "status": st,
+                     "plan": {k: plan[k] for k in ("producer", "BM", "BN", "stages", "cta_pair", "units",
+                                                   "split_tiles", "operand_copy")}})
     base = rows[0]["ms_per_step"]
     for r in rows:
-        r["speedup_vs_S1"] = base / r["ms_per_step"] if r["plan"]["cta_pair"] else None
-    print(json.dumps({"ablation": "ring depth and producer, 4096^3", "unit": "TFLOPS or TOPS per step",
+        r["speedup_vs_S1"] = base / r["ms_per_step"] if r["shape"] == list(SQUARE) and r["plan"]["cta_pair"] \
+            and r["config"].startswith("pair") else None
+    print(json.dumps({"ablation": "ring depth, producer and stream-K", "unit": "TFLOPS or TOPS",
                       "rows": rows}), flush=True)
     return 0
 
@@ -524,7 +538,7 @@ def main() -> int:
                     help="time dtype,M,N,K (s8 or f16) as the headline instead of INT8 4096^3 "
                          "(for profiling and sweeps; uniform inputs)")
     ap.add_argument("--force", default=None,
-                    help="plan override producer,bn,stages[,cta_pair] (see gemmpipe_set_plan_override)")
+                    help="plan override producer,bn,stages[,cta_pair[,split]] (see gemmpipe_set_plan_override)")
     ap.add_argument("--ablation", action="store_true",
                     help="ring-depth / producer ablation at 4096^3 instead of the benchmark line")
     args = ap.parse_args()

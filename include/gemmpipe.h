@@ -33,8 +33,14 @@
  * fp16, and misaligned fp16 operands of gemm_f16f32 padded to aligned rows --
  * allocated with cudaMalloc on first need, grown when a larger problem needs
  * it (cudaFree then waits for the device), released by
- * gemmpipe_release_workspaces() or at unload.  gemm_f16f32 with 16-byte
- * aligned operands and pitches allocates nothing.
+ * gemmpipe_release_workspaces() or at unload.  A second workspace per
+ * (device, stream) holds stream-K partial sums: when the output tiles do not
+ * divide evenly over the persistent grid, the k-blocks of the last waves'
+ * tiles are split into equal ranges over all CTAs and a split tile's parts
+ * are added by the CTA holding its last k-block (128 x BN x 4 bytes per CTA
+ * plus 64 KiB of flags; if it cannot be allocated, every tile runs whole
+ * instead -- same result, no error).  gemm_f16f32 with 16-byte aligned operands and pitches
+ * and a tile count that fills whole waves allocates nothing.
  *
  * Execution: every GEMM call is asynchronous on `stream` (a cudaStream_t;
  * NULL is the legacy default stream) and targets the current CUDA device.
@@ -106,8 +112,9 @@ typedef enum {
  * rounded up to a multiple of 8; calls on one stream share that stream's
  * workspace and are ordered by it.  With the plan override producer = 0 and
  * A, B on 16-byte boundaries with K and N multiples of 16, the kernel
- * instead loads int8 tiles and widens them in shared memory (nothing is
- * allocated; C also holds the running int32 sums between chunks).
+ * instead loads int8 tiles and widens them in shared memory (no operand
+ * copy; in single-CTA variants C also holds the running int32 sums between
+ * chunks).
  */
 GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K,
                                const int8_t *A, const int8_t *B, int32_t *C,
@@ -121,7 +128,8 @@ GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K,
  * A: M x K binary16, B: K x N binary16, C: M x N binary32.  Products are
  * accumulated in fp32 on the tensor cores; the summation order differs from
  * a sequential sum, so results agree with an fp64 reference to within fp32
- * accumulation error.  Allocates nothing.
+ * accumulation error.  Allocates only the stream-K workspace described
+ * above (and a padded copy of a misaligned operand).
  */
 GEMMPIPE_API gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K,
                               const gemmpipe_half_t *A, const gemmpipe_half_t *B,
@@ -204,13 +212,14 @@ typedef struct {
     int cta_pair;        /* 1: clusters of two CTAs share one 256-row MMA (tcgen05 cta_group::2) */
     int grid;            /* persistent CTAs launched */
     int64_t tiles;       /* output tiles of BM x BN */
-    int64_t tasks;       /* work items: tiles, with the last partial wave split into BN/2-wide halves */
+    int64_t units;       /* persistent units: CTAs, or CTA pairs */
+    int64_t split_tiles; /* tiles whose k-blocks are split over units (stream-K; 0: every tile whole) */
     int64_t k_blocks;    /* ceil(K / BK) */
     int64_t smem_bytes;  /* dynamic shared memory per CTA */
     int vector_store;    /* 1: 16-byte stores of C, 0: 4-byte stores */
     int operand_copy;    /* 0: none (INT8: widened in the kernel), 1: int8 widened to fp16 in the
                             workspace, 2: misaligned fp16 padded in the workspace */
-    int64_t workspace_bytes; /* library workspace the call needs */
+    int64_t workspace_bytes; /* library workspace the call needs (operand copies + split partial sums) */
 } gemmpipe_plan_t;
 
 /*
@@ -234,10 +243,12 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
  * ring depths (when the chosen variant has no such depth the automatic one
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
- * 0 single CTAs, 1 CTA pairs where the shape allows them.  Returns
+ * 0 single CTAs, 1 CTA pairs where the shape allows them.  split: -1
+ * automatic, 0 every tile whole (no stream-K split).  Returns
  * INVALID_VALUE for values outside these sets.
  */
-GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair);
+GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair,
+                                                          int split);
 
 /* Frees every INT8 workspace (synchronizes the device first). */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_release_workspaces(void);

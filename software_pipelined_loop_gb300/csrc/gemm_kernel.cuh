@@ -83,9 +83,19 @@ struct GemmCfg {
     static constexpr int CONV_GROUPS = CONV_GROUPS_;  // converter groups working on different k-blocks
     static_assert(CONV_WARPS == 0 || CONV_WARPS % CONV_GROUPS == 0, "groups of whole warps");
     static constexpr int MMA_WARP = PRODUCER_WARPS + CONV_WARPS;
-    static constexpr int EPI_WARP0 = MMA_WARP + 1;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = 32 * (PRODUCER_WARPS + CONV_WARPS + 1 + EPI_WARPS);
+    // Register split (TMA producer, no converter): warps 0-3 are the control
+    // warpgroup (producer, MMA issuer, two idle warps) and hand registers to
+    // the two epilogue warpgroups with setmaxnreg, so the INT8 epilogue
+    // keeps its 128 running sums per thread in registers.  The shares add up
+    // to the launch allocation of 384 threads x 168 registers.
+    static constexpr bool REG_SPLIT = !LDG && !CONVERT;
+    static constexpr int CTRL_REGS = 120;
+    static constexpr int EPI_REGS = 192;
+    static constexpr int EPI_WARP0 = REG_SPLIT ? 4 : MMA_WARP + 1;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    static constexpr int SPLIT_REGS = REG_SPLIT ? 32 * (4 * CTRL_REGS + EPI_WARPS * EPI_REGS) : 0;
+    static_assert(!REG_SPLIT || (THREADS == 384 && SPLIT_REGS == THREADS * 168), "register split shares");
     // Running int32 sums of the INT8 chunks: in registers (128 per epilogue
     // thread) while the CTA has at most 12 warps -- 3 per scheduler, 168
     // registers each; with more warps they are kept in C itself.
@@ -123,6 +133,18 @@ struct Ctl {
     int abort;
 };
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded mbarrier wait.  False when the CTA is aborting or the wait ran out
 // of time (then it records the timeout and raises the abort flag).
 struct Waiter {
@@ -147,6 +169,26 @@ struct Waiter {
         }
     }
 
+    // Bounded wait until a global flag holds `epoch` (another unit's
+    // partial sums are published).
+    __device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch) const
+    {
+        if (ld_acquire_u32(flag) == epoch) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            if (ld_acquire_u32(flag) == epoch) return true;
+            __nanosleep(64);
+            if ((i & 15u) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    *abort = 1;
+                    atomicCAS(status, 0, kStatusTimeout);
+                    return false;
+                }
+            }
+        }
+    }
+
     // Used only while draining after an abort: ignores the abort flag.
     __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) const
     {
@@ -159,38 +201,75 @@ struct Waiter {
 
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
-// Work of one task: an output tile at (m0, n0) that is BN or BN/2 wide.
-// Tasks [0, full_tasks) are whole tiles in m-fastest order; the tiles after
-// them (the last, partial wave of a persistent grid) are split into two
-// half-width tasks each, so the last wave has more, shorter tasks.
-struct Task {
+// One item of a unit's schedule: the k-blocks [kb0, kb1) of the output tile
+// at (m0, n0).  kind 0: the whole tile; 1: a part of a split tile that ends
+// before its last k-block (partial sums go to the unit's slot); 2: the part
+// holding the last k-block (this unit adds the other parts and stores C).
+struct Work {
     int64_t m0, n0;
-    int bn;
+    int64_t kb0, kb1;
+    int64_t sk_tile;  // index among the split tiles
+    int kind;
 };
 
+// Persistent schedule: unit = CTA (or CTA pair) index.
 template <class Cfg>
-__device__ __forceinline__ Task task_of(const GemmParams &p, int64_t u)
-{
-    if (u < p.full_tasks) {
-        return Task{(u % p.m_tiles) * Cfg::TILE_M, (u / p.m_tiles) * Cfg::BN, Cfg::BN};
-    }
-    const int64_t h = u - p.full_tasks;
-    const int64_t t = p.full_tasks + (h >> 1);
-    return Task{(t % p.m_tiles) * Cfg::TILE_M, (t / p.m_tiles) * Cfg::BN + (h & 1) * (Cfg::BN / 2), Cfg::BN / 2};
-}
-
-// Persistent schedule: a CTA (or a CTA pair) takes tasks first, first+step, ...
-template <class Cfg>
-__device__ __forceinline__ int64_t first_task()
+__device__ __forceinline__ int64_t unit_index()
 {
     return Cfg::PAIR ? (blockIdx.x >> 1) : blockIdx.x;
 }
 
-template <class Cfg>
-__device__ __forceinline__ int64_t task_step()
+// Start of a unit's range of split k-blocks (units[u] covers
+// [sk_begin(u), sk_begin(u + 1)) of the tile-major split work).
+__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int64_t unit)
 {
-    return Cfg::PAIR ? (gridDim.x >> 1) : gridDim.x;
+    return p.sk_work * unit / p.units;
 }
+
+// A unit's items: its whole tiles (round-robin over units), then its split
+// range from the last tile to the first.  The range's last item is the only
+// one that can end inside a tile (kind 1), so it is published first; its
+// first item, the only one that can hold a tile's last k-block after
+// another unit's part (kind 2), comes last and waits only on lower units.
+template <class Cfg>
+struct WorkIter {
+    int64_t dp, beg, pos;
+
+    __device__ __forceinline__ explicit WorkIter(const GemmParams &p)
+    {
+        const int64_t u = unit_index<Cfg>();
+        dp = u;
+        beg = sk_begin(p, u);
+        pos = sk_begin(p, u + 1);
+    }
+
+    __device__ __forceinline__ bool next(const GemmParams &p, Work &w)
+    {
+        int64_t tile;
+        if (dp < p.dp_tiles) {
+            tile = dp;
+            dp += p.units;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.kind = 0;
+            w.sk_tile = -1;
+        } else if (pos > beg) {
+            const int64_t t = (pos - 1) / p.num_kb;
+            const int64_t ts = t * p.num_kb;
+            w.kb1 = pos - ts;
+            w.kb0 = beg > ts ? beg - ts : 0;
+            pos = ts + w.kb0;
+            w.kind = w.kb1 < p.num_kb ? 1 : (w.kb0 > 0 ? 2 : 0);
+            w.sk_tile = t;
+            tile = p.dp_tiles + t;
+        } else {
+            return false;
+        }
+        w.m0 = (tile % p.m_tiles) * Cfg::TILE_M;
+        w.n0 = (tile / p.m_tiles) * Cfg::BN;
+        return true;
+    }
+};
 
 // ------------------------------------------------------------ TMA producer
 
@@ -200,7 +279,6 @@ __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, cons
 {
     // int8 tiles into this CTA's int8 ring: A box 64 (k) x 128 (rows), no
     // swizzle; B as atoms of 128 (n) x 64 (k) with the 128-byte swizzle.
-    // Always whole boxes (half-width tasks widen only the columns they use).
     // In a CTA pair each CTA loads its own rows of A and half of B.
     const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
     int stage = 0;
@@ -208,11 +286,12 @@ __device__ void producer_tma_i8(const GemmParams &p, const CUtensorMap *tA, cons
     uint32_t armed = 0, armed_par = 0;
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
-        const Task tk = task_of<Cfg>(p, u);
-        const int32_t m0 = static_cast<int32_t>(tk.m0 + rank * Cfg::BM);
-        const int32_t n0 = static_cast<int32_t>(tk.n0 + rank * (tk.bn / 2));
-        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (ok && it.next(p, wk)) {
+        const int32_t m0 = static_cast<int32_t>(wk.m0 + rank * Cfg::BM);
+        const int32_t n0 = static_cast<int32_t>(wk.n0 + rank * Cfg::CTA_BN);
+        for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty_i8[stage]), phase ^ 1u)) {
                 ok = false;
                 break;
@@ -299,9 +378,10 @@ __device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, 
     // the leader's full barrier.
     const bool to_leader = Cfg::PAIR;
     int64_t kcount = 0;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
-        const int bn = Cfg::PAIR ? task_of<Cfg>(p, u).bn / 2 : task_of<Cfg>(p, u).bn;  // this CTA's columns
-        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kcount) {
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (it.next(p, wk)) {
+        for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kcount) {
             if (kcount % G != g) continue;
             const int si = static_cast<int>(kcount % Cfg::I8_STAGES);
             const uint32_t phi = static_cast<uint32_t>((kcount / Cfg::I8_STAGES) & 1);
@@ -345,11 +425,9 @@ __device__ void converter(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGES, 
                     } else {
                         const int pc = gt + (b0 + i - A_PIECES / GT) * GT;
                         const int kk = pc % Cfg::BK, jn = pc / Cfg::BK;  // k row, 16-n piece
-                        if (jn * 16 < bn) {
-                            const uint32_t row = fb + (jn >> 2) * 8192 + kk * 128;
-                            const int c0 = (jn & 3) * 2;
-                            widen16_store(v[i], row + ((c0 ^ (kk & 7)) << 4), row + (((c0 + 1) ^ (kk & 7)) << 4));
-                        }
+                        const uint32_t row = fb + (jn >> 2) * 8192 + kk * 128;
+                        const int c0 = (jn & 3) * 2;
+                        widen16_store(v[i], row + ((c0 ^ (kk & 7)) << 4), row + (((c0 + 1) ^ (kk & 7)) << 4));
                     }
                 }
             }
@@ -377,13 +455,12 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
     uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arm
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
-        const Task tk = task_of<Cfg>(p, u);
-        const int32_t m0 = static_cast<int32_t>(tk.m0);
-        const int32_t n0 = static_cast<int32_t>(tk.n0);
-        const int nb64 = tk.bn / 64;
-        const uint32_t stage_bytes = Cfg::A_BYTES + tk.bn * Cfg::BK * 2;
-        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (ok && it.next(p, wk)) {
+        const int32_t m0 = static_cast<int32_t>(wk.m0);
+        const int32_t n0 = static_cast<int32_t>(wk.n0);
+        for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
                 ok = false;
                 break;
@@ -392,11 +469,10 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
                 const uint32_t fb = smem_u32(&ctl->full[stage]);
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
-                mbar_arrive_expect_tx(fb, stage_bytes);
+                mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
                 tma_load_2d(sa, tA, fb, k0, m0);
 #pragma unroll
-                for (int j = 0; j < Cfg::NB64; ++j)
-                    if (j < nb64) tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -495,12 +571,12 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
     int stage = 0;
     uint32_t phase = 0;
     int64_t kb_count = 0;
-    // The host gives this producer whole tiles only (full_tasks == tasks).
-    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
-        const Task tk = task_of<Cfg>(p, u);
-        const int64_t m0 = tk.m0;
-        const int64_t n0 = tk.n0;
-        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (it.next(p, wk)) {
+        const int64_t m0 = wk.m0;
+        const int64_t n0 = wk.n0;
+        for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             const int64_t k0 = kb * Cfg::BK;
             const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
             const uint32_t sb = sa + Cfg::A_BYTES;
@@ -563,14 +639,13 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     uint32_t armed = 0, armed_par = 0;
     int64_t kb_count = 0;
     bool ok = true;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
-        const Task tk = task_of<Cfg>(p, u);
-        const int32_t m0 = static_cast<int32_t>(tk.m0 + rank * Cfg::BM);
-        const int half = tk.bn / 2;  // B columns this CTA loads
-        const int32_t n0 = static_cast<int32_t>(tk.n0 + rank * half);
-        const int natoms = half / 64;
-        const uint32_t pair_bytes = 2u * (Cfg::A_BYTES + half * Cfg::BK * 2);
-        for (int64_t kb = 0; kb < p.num_kb; ++kb, ++kb_count) {
+    constexpr uint32_t pair_bytes = 2u * Cfg::STAGE_BYTES;  // both CTAs' copies
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (ok && it.next(p, wk)) {
+        const int32_t m0 = static_cast<int32_t>(wk.m0 + rank * Cfg::BM);
+        const int32_t n0 = static_cast<int32_t>(wk.n0 + rank * Cfg::CTA_BN);  // this CTA's half of B
+        for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
                 ok = false;
                 break;
@@ -583,8 +658,7 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
                 tma_load_2d_pair(sa, tA, fb, k0, m0);
 #pragma unroll
-                for (int j = 0; j < Cfg::NB64; ++j)
-                    if (j < natoms) tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -615,17 +689,17 @@ template <class Cfg>
 __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
                                 Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
-    constexpr uint32_t IDESC_FULL = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN, true);
-    constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN / 2, true);
+    constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN, true);
     constexpr uint16_t BOTH = 3;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
-        const uint32_t idesc = task_of<Cfg>(p, u).bn == Cfg::BN ? IDESC_FULL : IDESC_HALF;
-        for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
-            const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (ok && it.next(p, wk)) {
+        for (int64_t kc = wk.kb0; kc < wk.kb1 && ok; kc += p.kb_per_chunk) {
+            const int64_t kend = kc + p.kb_per_chunk < wk.kb1 ? kc + p.kb_per_chunk : wk.kb1;
             if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
                 ok = false;
                 break;
@@ -671,16 +745,16 @@ template <class Cfg>
 __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
                            Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
-    constexpr uint32_t IDESC_FULL = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
-    constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(Cfg::BM, Cfg::BN / 2, true);
+    constexpr uint32_t idesc = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks && ok; u += task_step<Cfg>()) {
-        const uint32_t idesc = task_of<Cfg>(p, u).bn == Cfg::BN ? IDESC_FULL : IDESC_HALF;
-        for (int64_t kc = 0; kc < p.num_kb && ok; kc += p.kb_per_chunk) {
-            const int64_t kend = kc + p.kb_per_chunk < p.num_kb ? kc + p.kb_per_chunk : p.num_kb;
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (ok && it.next(p, wk)) {
+        for (int64_t kc = wk.kb0; kc < wk.kb1 && ok; kc += p.kb_per_chunk) {
+            const int64_t kend = kc + p.kb_per_chunk < wk.kb1 ? kc + p.kb_per_chunk : wk.kb1;
             if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
                 ok = false;
                 break;
@@ -800,6 +874,59 @@ __device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, c
     __syncwarp();
 }
 
+// Partial-sum slots of split tiles: slot = CTA (2 * pair + rank for pairs),
+// 128 x BN values as [epilogue warp][32-column block][32 x 32].  Within a
+// block the 16-byte group i of lane l's row sits at uint4 index 32 i + l, so
+// every access of a warp covers 512 contiguous bytes.
+template <class Cfg>
+__device__ __forceinline__ uint4 *part_block(const GemmParams &p, int64_t slot, int e, int jb)
+{
+    return reinterpret_cast<uint4 *>(p.partials + slot * (Cfg::BM * Cfg::BN) +
+                                     (static_cast<int64_t>(e) * (Cfg::EPI_COLS / 32) + jb) * 1024);
+}
+
+template <class Cfg>
+__device__ __forceinline__ int64_t slot_of(int64_t unit, uint32_t rank)
+{
+    return Cfg::PAIR ? 2 * unit + rank : unit;
+}
+
+__device__ __forceinline__ void write_part(uint4 *blk, const uint32_t *r, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) blk[32 * i + lane] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+}
+
+template <bool INT>
+__device__ __forceinline__ void add_part(const uint4 *blk, uint32_t *r, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = blk[32 * i + lane];
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (INT)
+                r[4 * i + j] += x[j];
+            else
+                r[4 * i + j] = __float_as_uint(__uint_as_float(r[4 * i + j]) + __uint_as_float(x[j]));
+        }
+    }
+}
+
+// The lowest unit whose range holds k-blocks of split tile `sk_tile`.  The
+// units from there up to this one's predecessor hold its earlier k-blocks
+// (every range is non-empty: the split work has at least one k-block per
+// unit).
+template <class Cfg>
+__device__ __forceinline__ int64_t first_part_unit(const GemmParams &p, int64_t sk_tile)
+{
+    const int64_t tile_start = sk_tile * p.num_kb;
+    int64_t v = unit_index<Cfg>() - 1;
+    while (v > 0 && sk_begin(p, v) > tile_start) --v;
+    return v;
+}
+
 template <class Cfg>
 __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
                          const Waiter &w, int warp, int lane, uint32_t rank)
@@ -807,64 +934,83 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
     const int e = warp - Cfg::EPI_WARP0;  // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int h = e >> 2;                  // column half of the tile
+    constexpr int NCOLS = Cfg::EPI_COLS;   // this warp's columns
+    constexpr bool INT = Cfg::INT_OUT;
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
+    const int64_t me = unit_index<Cfg>();
+    const int64_t my_slot = slot_of<Cfg>(me, rank);
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t u = first_task<Cfg>(); u < p.tasks; u += task_step<Cfg>()) {
-        const Task tk = task_of<Cfg>(p, u);
-        const int ncols = tk.bn / 2;  // this warp's columns
-        const int64_t row0 = tk.m0 + rank * Cfg::BM + q * 32;
-        const int64_t colb = tk.n0 + h * ncols;
-        uint32_t isum[(Cfg::INT_OUT && !Cfg::SUM_IN_C) ? Cfg::EPI_COLS : 1];
-        if constexpr (Cfg::INT_OUT && !Cfg::SUM_IN_C) {
-#pragma unroll
-            for (int i = 0; i < Cfg::EPI_COLS; ++i) isum[i] = 0;
+    WorkIter<Cfg> it(p);
+    Work wk;
+    while (it.next(p, wk)) {
+        const int64_t row0 = wk.m0 + rank * Cfg::BM + q * 32;
+        const int64_t colb = wk.n0 + h * NCOLS;
+        int64_t v_lo = me;
+        if (wk.kind == 2) {
+            // The other parts of this split tile must be published before
+            // they are added.  Each is the first split item of a lower unit,
+            // which waits on nothing to produce it.
+            v_lo = first_part_unit<Cfg>(p, wk.sk_tile);
+            bool got = true;
+            for (int64_t v = me - 1; v >= v_lo && got; --v)
+                got = w.wait_flag(&p.flags[slot_of<Cfg>(v, rank) * Cfg::EPI_WARPS + e], p.epoch);
+            if (!__all_sync(0xffffffffu, got)) return;
         }
-        for (int64_t kc = 0; kc < p.num_kb; kc += p.kb_per_chunk) {
+        uint32_t isum[(INT && !Cfg::SUM_IN_C) ? NCOLS : 1];
+        if constexpr (INT && !Cfg::SUM_IN_C) {
+            // Integer sums: the other parts of a split tile can start them
+            // (the order of exact additions does not matter).
+#pragma unroll
+            for (int i = 0; i < NCOLS; ++i) isum[i] = 0;
+            for (int64_t v = me - 1; v >= v_lo; --v)
+#pragma unroll
+                for (int jb = 0; jb < NCOLS / 32; ++jb)
+                    add_part<true>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), &isum[jb * 32], lane);
+        }
+        for (int64_t kc = wk.kb0; kc < wk.kb1; kc += p.kb_per_chunk) {
             const bool got = w.wait(smem_u32(&ctl->tfull[acc]), acc_phase);
             if (!__all_sync(0xffffffffu, got)) return;
             tc_fence_after_sync();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * ncols;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * NCOLS;
             if constexpr (Cfg::SUM_IN_C) {
-                // Chunk partials are exact integers; the first chunk stores
-                // them, later chunks add into C (each element is read and
-                // written by the same thread, in chunk order).
+                // Whole tiles only.  Chunk partials are exact integers; the
+                // first chunk stores them, later chunks add into C (each
+                // element is read and written by the same thread, in order).
 #pragma unroll
-                for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
-                    if (jb < ncols / 32) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + jb * 32, r);
-                        tmem_wait_ld();
+                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-                        if (kc == 0)
-                            store_block<false>(p, stg, r, row0, colb + jb * 32, lane);
-                        else
-                            store_block<true>(p, stg, r, row0, colb + jb * 32, lane);
-                    }
+                    for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+                    if (kc == wk.kb0)
+                        store_block<false>(p, stg, r, row0, colb + jb * 32, lane);
+                    else
+                        store_block<true>(p, stg, r, row0, colb + jb * 32, lane);
                 }
-            } else if constexpr (Cfg::INT_OUT) {
+            } else if constexpr (INT) {
                 // Chunk partials are integers below 2^24 in magnitude: exact
-                // in fp32, so the conversion is exact.  16 columns per load
-                // keep the 128 running sums in registers.
+                // in fp32, so the conversion is exact.
 #pragma unroll
-                for (int jb = 0; jb < Cfg::EPI_COLS / 16; ++jb) {
-                    if (jb < ncols / 16) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(tbase + jb * 16, r);
-                        tmem_wait_ld();
+                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            isum[jb * 16 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        isum[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
                 }
             } else {
 #pragma unroll
-                for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb) {
-                    if (jb < ncols / 32) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + jb * 32, r);
-                        tmem_wait_ld();
+                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + jb * 32, r);
+                    tmem_wait_ld();
+                    if (wk.kind == 1) {
+                        write_part(part_block<Cfg>(p, my_slot, e, jb), r, lane);
+                    } else {
+                        for (int64_t v = me - 1; v >= v_lo; --v)
+                            add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), r, lane);
                         store_block(p, stg, r, row0, colb + jb * 32, lane);
                     }
                 }
@@ -880,10 +1026,20 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if constexpr (Cfg::INT_OUT && !Cfg::SUM_IN_C) {
+        if constexpr (INT && !Cfg::SUM_IN_C) {
 #pragma unroll
-            for (int jb = 0; jb < Cfg::EPI_COLS / 32; ++jb)
-                if (jb < ncols / 32) store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
+            for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                if (wk.kind == 1)
+                    write_part(part_block<Cfg>(p, my_slot, e, jb), &isum[jb * 32], lane);
+                else
+                    store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
+            }
+        }
+        if (wk.kind == 1) {
+            // Publish this warp's part: data first, then the flag.
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_u32(&p.flags[my_slot * Cfg::EPI_WARPS + e], p.epoch);
         }
     }
 }
@@ -943,16 +1099,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t tmem_base = ctl->tmem_base;
     const Waiter w{&ctl->abort, p.status, p.timeout_ns};
     const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
-
-    if (warp < Cfg::PRODUCER_WARPS) {
+    if constexpr (Cfg::REG_SPLIT) {
+        // Each role runs inside the branch that set its register share.
+        if (warp < 4) {
+            setmaxnreg_dec<Cfg::CTRL_REGS>();
+            if (warp == 0) {
+                if (lane == 0) {
+                    if constexpr (Cfg::PAIR)
+                        producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
+                    else
+                        producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
+                }
+            } else if (warp == Cfg::MMA_WARP) {
+                if constexpr (Cfg::PAIR) {
+                    if (lane == 0 && rank == 0) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w);
+                } else {
+                    if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+                }
+                __syncwarp();
+            }
+        } else {
+            setmaxnreg_inc<Cfg::EPI_REGS>();
+            epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane, rank);
+        }
+    } else if (warp < Cfg::PRODUCER_WARPS) {
         if constexpr (Cfg::LDG) {
             producer_ldg<Cfg>(p, sbase, ctl, w);
         } else if constexpr (Cfg::CONVERT) {
             if (lane == 0) producer_tma_i8<Cfg>(p, &tmA, &tmB, sbase, ctl, w);  // single CTA or pair
-        } else if constexpr (Cfg::PAIR) {
-            if (lane == 0) producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
-        } else {
-            if (lane == 0) producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
         }
     } else if (warp < Cfg::MMA_WARP) {
         if constexpr (Cfg::CONVERT) converter<Cfg>(p, sbase, ctl, w);

@@ -14,9 +14,20 @@ struct GemmParams {
     int64_t ldb;
     void *C;  // float or int32, M x N, row pitch ldc elements
     int64_t ldc;
-    int64_t m_tiles, tiles;  // BM x BN tile grid (m fastest)
-    int64_t full_tasks;      // tasks that are whole tiles: [0, full_tasks)
-    int64_t tasks;           // whole tiles, then the tail tiles split into two BN/2 halves
+    int64_t m_tiles, tiles;  // tile grid (m fastest); a tile is 128 or 256 (CTA pair) rows x BN
+    // Persistent schedule over `units` (CTAs, or CTA pairs): tiles
+    // [0, dp_tiles) go whole and round-robin; the k-blocks of the remaining
+    // tiles (sk_work = their count times num_kb, tile-major) are split into
+    // `units` equal contiguous ranges ("stream-K").  A unit whose range does
+    // not start a tile leaves its partial sums in `partials` (one slot per
+    // CTA) and publishes them with `epoch` in `flags`; the unit holding the
+    // tile's first k-block adds them and stores C.
+    int64_t units;
+    int64_t dp_tiles;
+    int64_t sk_work;
+    uint32_t epoch;
+    uint32_t *partials;  // fp32 or int32 values, 128 x BN per slot
+    uint32_t *flags;     // one per (slot, epilogue warp)
     int64_t num_kb;        // ceil(K / BK)
     int64_t kb_per_chunk;  // k-blocks per TMEM accumulation unit
     int vec_store;         // C base and pitch allow 16-byte stores

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -112,7 +113,7 @@ gemmpipe_status_t check_device_pointers(int64_t K, const void *A, const void *B,
 // ------------------------------------------------------------------ plans
 
 struct Override {
-    int producer = -1, bn = 0, stages = 0, pair = -1;
+    int producer = -1, bn = 0, stages = 0, pair = -1, split = -1;
 };
 Override g_override;
 
@@ -125,9 +126,40 @@ StallHook g_stall;
 struct Plan {
     const Variant *v = nullptr;
     int grid = 0;
-    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0, full_tasks = 0, tasks = 0;
+    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0;
+    int64_t units = 0, dp_tiles = 0, sk_tiles = 0;
+    int64_t slots = 0;  // co-resident units (CTAs or CTA pairs)
     int vec_store = 0;
+    int64_t split_ctas() const { return v->info.pair ? 2 * units : units; }
+    int64_t split_bytes() const;  // stream-K partials + flags (0: none)
+    void run_whole_tiles()
+    {
+        units = tiles < slots ? tiles : slots;
+        dp_tiles = tiles;
+        sk_tiles = 0;
+        grid = static_cast<int>(v->info.pair ? 2 * units : units);
+    }
 };
+
+// Stream-K flags: one per epilogue warp of each CTA, in a fixed region at
+// the start of the split workspace that holds nothing but epochs (partial
+// sums of a plan with a larger grid never land where a flag of another plan
+// is read), so a flag equals the current epoch only once this launch has
+// published it.  Launches beyond kMaxSplitCtas CTAs run whole tiles.
+constexpr int64_t kSplitFlagsPerCta = 8;
+constexpr int64_t kMaxSplitCtas = 2048;
+constexpr int64_t kSplitFlagBytes = kMaxSplitCtas * kSplitFlagsPerCta * 4;
+
+// Fewest k-blocks a stream-K unit is given when tiles alone cannot fill the
+// grid: below this the ring's fill and the fix-up cost more than the idle
+// SMs they replace.
+constexpr int64_t kMinSplitKb = 8;
+
+int64_t Plan::split_bytes() const
+{
+    if (sk_tiles == 0) return 0;
+    return kSplitFlagBytes + split_ctas() * static_cast<int64_t>(v->info.BM) * v->info.BN * 4;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -164,7 +196,7 @@ bool s8_convert_ok(const void *A, int64_t K, const void *B, int64_t N)
 // convert is true.
 gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                             const void *B, int64_t ldb, const void *C, int64_t ldc, const DeviceInfo &d, Plan *pl,
-                            bool convert = false)
+                            bool convert = false, bool split_ok = true)
 {
     Override ov;
     {
@@ -195,19 +227,30 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
-    // Persistent grid: one CTA (or CTA pair) per SM (pair) slot.
+    // Persistent grid: at most one CTA (or CTA pair) per SM (pair) slot.
+    // Whole tiles go round-robin; when they leave a partial last wave, that
+    // wave and the one before it are spread over all units as equal ranges
+    // of k-blocks (stream-K), so every unit does the same work.  With fewer
+    // tiles than slots, all tiles are split over as many units as keep at
+    // least kMinSplitKb k-blocks each.
     const int64_t slots = v->info.pair ? v->max_pairs() : d.sms;
-    const int64_t units = pl->tiles < slots ? pl->tiles : slots;
-    pl->grid = static_cast<int>(v->info.pair ? 2 * units : units);
-    // Balance the last wave: if the tiles left after the full waves fit
-    // twice over into the grid, each is done as two half-width tasks.
-    const int64_t rem = pl->tiles % units;
-    pl->full_tasks = pl->tiles;
-    pl->tasks = pl->tiles;
-    if (v->info.producer == 0 && rem > 0 && 2 * rem <= units && pl->tiles > units) {
-        pl->full_tasks = pl->tiles - rem;
-        pl->tasks = pl->tiles + rem;
+    const int64_t T = pl->tiles;
+    const bool split = split_ok && v->info.split_ok && ov.split != 0;
+    pl->slots = slots;
+    pl->run_whole_tiles();
+    if (split && T < slots) {
+        const int64_t want = (T * pl->num_kb + kMinSplitKb - 1) / kMinSplitKb;
+        const int64_t u = want < slots ? want : slots;
+        if (u > T) {
+            pl->units = u;
+            pl->dp_tiles = 0;
+            pl->sk_tiles = T;
+        }
+    } else if (split && T % slots != 0 && pl->num_kb > 1) {
+        pl->sk_tiles = slots + T % slots;
+        pl->dp_tiles = T - pl->sk_tiles;
     }
+    pl->grid = static_cast<int>(v->info.pair ? 2 * pl->units : pl->units);
     pl->vec_store = aligned16(C) && (ldc * 4) % 16 == 0;
     return GEMMPIPE_OK;
 }
@@ -314,12 +357,18 @@ struct Workspace {
     void *ptr = nullptr;
     int64_t bytes = 0;
 };
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+// Kinds of workspace per (device, stream).
+enum WsKind { kWsOperands = 0, kWsSplit = 1 };
+std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 
-gemmpipe_status_t workspace(int dev, cudaStream_t s, int64_t bytes, void **out)
+// The (device, stream) workspace of one kind, at least `bytes` long.  A new
+// stream-K workspace has its flags (the first zero_bytes bytes) zeroed on
+// the stream before first use.
+gemmpipe_status_t workspace(int dev, cudaStream_t s, int64_t bytes, void **out, int kind = kWsOperands,
+                            int64_t zero_bytes = 0)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    Workspace &w = g_ws[{dev, s}];
+    Workspace &w = g_ws[std::make_tuple(dev, s, kind)];
     if (w.bytes < bytes) {
         if (w.ptr) {
             cudaFree(w.ptr);  // synchronizes: earlier users of the buffer have finished
@@ -332,6 +381,14 @@ gemmpipe_status_t workspace(int dev, cudaStream_t s, int64_t bytes, void **out)
             return GEMMPIPE_ERR_OUT_OF_MEMORY;
         }
         w.bytes = bytes;
+        if (zero_bytes > 0 && cudaMemsetAsync(w.ptr, 0, static_cast<size_t>(zero_bytes), s) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            return GEMMPIPE_ERR_LAUNCH;
+        }
     }
     *out = w.ptr;
     return GEMMPIPE_OK;
@@ -339,8 +396,41 @@ gemmpipe_status_t workspace(int dev, cudaStream_t s, int64_t bytes, void **out)
 
 // ------------------------------------------------------------------- runs
 
-gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, int64_t K, const uint16_t *A,
-                           int64_t lda, const uint16_t *B, int64_t ldb, void *C, int64_t ldc, cudaStream_t s)
+std::atomic<uint32_t> g_epoch{0};
+
+// Fills the stream-K fields of p: the split tiles' partial sums and flags in
+// the stream's split workspace, and a fresh epoch.  Without that workspace
+// the plan falls back to whole tiles.
+void set_schedule(Plan &pl, int dev, cudaStream_t s, GemmParams &p)
+{
+    p.partials = nullptr;
+    p.flags = nullptr;
+    p.epoch = 0;
+    if (pl.sk_tiles > 0) {
+        void *ws = nullptr;
+        if (pl.split_ctas() <= kMaxSplitCtas &&
+            workspace(dev, s, pl.split_bytes(), &ws, kWsSplit, kSplitFlagBytes) == GEMMPIPE_OK) {
+            p.flags = static_cast<uint32_t *>(ws);
+            p.partials = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kSplitFlagBytes);
+            uint32_t e = g_epoch.fetch_add(1) + 1;
+            if (e == 0) e = g_epoch.fetch_add(1) + 1;  // 0 is the zeroed flags' value
+            p.epoch = e;
+        } else {
+            pl.run_whole_tiles();
+        }
+    }
+    p.m_tiles = pl.m_tiles;
+    p.tiles = pl.tiles;
+    p.units = pl.units;
+    p.dp_tiles = pl.dp_tiles;
+    p.sk_work = pl.sk_tiles * pl.num_kb;
+    p.num_kb = pl.num_kb;
+    p.kb_per_chunk = pl.kb_per_chunk;
+    p.vec_store = pl.vec_store;
+}
+
+gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
+                           const uint16_t *B, int64_t ldb, void *C, int64_t ldc, cudaStream_t s)
 {
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
@@ -366,13 +456,7 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
     p.ldb = ldb;
     p.C = C;
     p.ldc = ldc;
-    p.m_tiles = pl.m_tiles;
-    p.tiles = pl.tiles;
-    p.full_tasks = pl.full_tasks;
-    p.tasks = pl.tasks;
-    p.num_kb = pl.num_kb;
-    p.kb_per_chunk = pl.kb_per_chunk;
-    p.vec_store = pl.vec_store;
+    set_schedule(pl, dev, s, p);
     p.stall_kb = -1;
     p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
     {
@@ -392,7 +476,6 @@ gemmpipe_status_t run_plan(const Plan &pl, bool int_out, int64_t M, int64_t N, i
     tr.end();
     if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
-    (void)int_out;
     return GEMMPIPE_OK;
 }
 
@@ -472,7 +555,8 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
         return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
     Plan pl;
-    if ((st = make_plan(true, M, N, K, A16, Kp, B16, Np, C, N, d, &pl)) != GEMMPIPE_OK) return st;
+    // Whole tiles only: split tiles would need a partial-sum workspace.
+    if ((st = make_plan(true, M, N, K, A16, Kp, B16, Np, C, N, d, &pl, false, false)) != GEMMPIPE_OK) return st;
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
@@ -489,8 +573,12 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
     p.ldc = N;
     p.m_tiles = pl.m_tiles;
     p.tiles = pl.tiles;
-    p.full_tasks = pl.full_tasks;
-    p.tasks = pl.tasks;
+    p.units = pl.units;
+    p.dp_tiles = pl.dp_tiles;
+    p.sk_work = 0;
+    p.epoch = 0;
+    p.partials = nullptr;
+    p.flags = nullptr;
     p.num_kb = pl.num_kb;
     p.kb_per_chunk = pl.kb_per_chunk;
     p.vec_store = pl.vec_store;
@@ -553,7 +641,7 @@ gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_ha
     }
     Plan pl;
     if ((st = make_plan(false, M, N, K, Ause, lda, Buse, ldb, C, N, d, &pl)) != GEMMPIPE_OK) return st;
-    return run_plan(pl, false, M, N, K, Ause, lda, Buse, ldb, C, N, s);
+    return run_plan(pl, dev, M, N, K, Ause, lda, Buse, ldb, C, N, s);
 }
 
 gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B, int32_t *C,
@@ -573,7 +661,7 @@ gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A,
         const uint16_t *A8 = reinterpret_cast<const uint16_t *>(A);
         const uint16_t *B8 = reinterpret_cast<const uint16_t *>(B);
         if ((st = make_plan(true, M, N, K, A8, K, B8, N, C, N, d, &pl, true)) != GEMMPIPE_OK) return st;
-        return run_plan(pl, true, M, N, K, A8, K, B8, N, C, N, s);
+        return run_plan(pl, dev, M, N, K, A8, K, B8, N, C, N, s);
     }
     const int64_t Kp = round8(K), Np = round8(N);
     void *ws = nullptr;
@@ -589,7 +677,7 @@ gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A,
     }
     Plan pl;
     if ((st = make_plan(true, M, N, K, A16, Kp, B16, Np, C, N, d, &pl)) != GEMMPIPE_OK) return st;
-    return run_plan(pl, true, M, N, K, A16, Kp, B16, Np, C, N, s);
+    return run_plan(pl, dev, M, N, K, A16, Kp, B16, Np, C, N, s);
 }
 
 gemmpipe_status_t gemmpipe_get_device_status(gemmpipe_stream_t stream)
@@ -691,25 +779,29 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     plan->threads = f.threads;
     plan->grid = pl.grid;
     plan->tiles = pl.tiles;
-    plan->tasks = pl.tasks;
+    plan->units = pl.units;
+    plan->split_tiles = pl.sk_tiles;
     plan->k_blocks = pl.num_kb;
     plan->smem_bytes = f.smem_bytes;
     plan->vector_store = pl.vec_store;
+    plan->workspace_bytes += pl.split_bytes();
 
     return GEMMPIPE_OK;
 }
 
-gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair)
+gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair, int split)
 {
     if (producer < -1 || producer > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
     if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (split < -1 || split > 0) return GEMMPIPE_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_override.producer = producer;
     g_override.bn = bn;
     g_override.stages = stages;
     g_override.pair = cta_pair;
+    g_override.split = split;
     return GEMMPIPE_OK;
 }
 
@@ -720,7 +812,7 @@ gemmpipe_status_t gemmpipe_release_workspaces(void)
     const bool have = cudaGetDevice(&cur) == cudaSuccess;
     for (auto &kv : g_ws) {
         if (kv.second.ptr) {
-            cudaSetDevice(kv.first.first);
+            cudaSetDevice(std::get<0>(kv.first));
             cudaFree(kv.second.ptr);
         }
     }

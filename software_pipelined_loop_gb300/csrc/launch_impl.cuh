@@ -20,6 +20,16 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmPar
         e = cudaFuncSetAttribute(gemm_pipelined_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if constexpr (Cfg::REG_SPLIT) {
+            // setmaxnreg.inc waits until the CTA's launch allocation can
+            // cover the warpgroups' new shares: refuse a build whose
+            // allocation is smaller instead of launching a kernel that
+            // would wait forever.
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, gemm_pipelined_kernel<Cfg>);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs * Cfg::THREADS < Cfg::SPLIT_REGS) return cudaErrorInvalidConfiguration;
+        }
         attr_done[dev].store(1);
     }
     if constexpr (Cfg::PAIR) {
@@ -91,7 +101,8 @@ template <class Cfg>
 constexpr Variant make_variant()
 {
     return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::CONVERT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK,
-                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::PAIR ? 1 : 0, Cfg::THREADS, Cfg::SMEM_BYTES},
+                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::PAIR ? 1 : 0, Cfg::THREADS, Cfg::SMEM_BYTES,
+                    Cfg::SUM_IN_C ? 0 : 1},
                    &launch_cfg<Cfg>, &max_pairs_cfg<Cfg>};
 }
 

@@ -385,4 +385,18 @@ __device__ __forceinline__ void realign16(const uint4 &lo, const uint4 &hi, uint
     o[3] = __funnelshift_r(a3, a4, sh);
 }
 
+// Warpgroup register reallocation (all four warps of a warpgroup execute
+// it, converged).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 }  // namespace gp

@@ -18,6 +18,7 @@ struct VariantInfo {
     int pair;  // 1: cluster of two CTAs, tcgen05.mma.cta_group::2, 256-row tiles
     int threads;
     int smem_bytes;
+    int split_ok;  // 1: the epilogue can take split (stream-K) tiles
 };
 
 using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const GemmParams &, int grid,

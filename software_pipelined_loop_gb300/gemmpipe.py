@@ -33,7 +33,8 @@ class GemmpipeError(RuntimeError):
 class PlanT(ctypes.Structure):
     _fields_ = [("producer", ctypes.c_int), ("BM", ctypes.c_int), ("BN", ctypes.c_int), ("BK", ctypes.c_int),
                 ("stages", ctypes.c_int), ("k_chunk", ctypes.c_int), ("threads", ctypes.c_int),
-                ("cta_pair", ctypes.c_int), ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("tasks", ctypes.c_int64),
+                ("cta_pair", ctypes.c_int), ("grid", ctypes.c_int), ("tiles", ctypes.c_int64), ("units", ctypes.c_int64),
+                ("split_tiles", ctypes.c_int64),
                 ("k_blocks", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("vector_store", ctypes.c_int),
                 ("operand_copy", ctypes.c_int), ("workspace_bytes", ctypes.c_int64)]
@@ -60,7 +61,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gemmpipe_compute_load_ratio": (ctypes.c_double, [_int, _int, _int, _int]),
         "gemmpipe_stage_smem_bytes": (_i64, [_int, _int, _int, _int, _int]),
         "gemmpipe_plan": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.POINTER(PlanT)]),
-        "gemmpipe_set_plan_override": (_int, [_int, _int, _int, _int]),
+        "gemmpipe_set_plan_override": (_int, [_int, _int, _int, _int, _int]),
         "gemmpipe_release_workspaces": (_int, []),
         "gemmpipe_timing_enable": (_int, [_int]),
         "gemmpipe_timing_read": (_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
@@ -149,8 +150,9 @@ def gemmpipe_plan(dtype: int, M, N, K, A=None, B=None, C=None) -> dict:
     return {name: getattr(p, name) for name, _ in PlanT._fields_}
 
 
-def gemmpipe_set_plan_override(producer: int = -1, bn: int = 0, stages: int = 0, cta_pair: int = -1) -> None:
-    _check(load().gemmpipe_set_plan_override(producer, bn, stages, cta_pair), "gemmpipe_set_plan_override")
+def gemmpipe_set_plan_override(producer: int = -1, bn: int = 0, stages: int = 0, cta_pair: int = -1,
+                               split: int = -1) -> None:
+    _check(load().gemmpipe_set_plan_override(producer, bn, stages, cta_pair, split), "gemmpipe_set_plan_override")
 
 
 def gemmpipe_release_workspaces() -> None:

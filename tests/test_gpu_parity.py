@@ -346,15 +346,15 @@ def test_copy_kernel(dev):
     assert torch.equal(odd[1:1000].cpu(), src.cpu().view(torch.uint8)[3:1002])
 
 
-# ---------------------------------------------------- last-wave task split
+# ------------------------------------------------ stream-K (split tiles)
 
 @pytest.mark.parametrize("dtype", ["f16", "s8"])
 @pytest.mark.parametrize("wide", [True, False], ids=["bn256", "bn128"])
 @pytest.mark.parametrize("n_extra", [0, 8], ids=["n16", "n8"])
 def test_tail_wave_split(dev, dtype, wide, n_extra):
-    # Tile counts a little above one wave of the persistent grid: the tiles of
-    # the last, partial wave run as two half-width tasks each.  Wide shapes
-    # run on CTA pairs (256-row tiles), N <= 128 on single CTAs.
+    # Tile counts a little above one wave of the persistent grid: the last
+    # two waves' tiles are split into equal k-block ranges over all units.
+    # Wide shapes run on CTA pairs (256-row tiles), N <= 128 on single CTAs.
     if wide:
         N, K, n_tiles = 496 + n_extra, 144, 2
     else:
@@ -368,13 +368,105 @@ def test_tail_wave_split(dev, dtype, wide, n_extra):
     plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
     tiles = m_tiles * n_tiles
     rem = tiles % units
-    assert plan["tiles"] == tiles
-    assert 0 < rem and 2 * rem <= units and plan["tasks"] == tiles + rem
+    assert plan["tiles"] == tiles and plan["units"] == units
+    assert 0 < rem and plan["split_tiles"] == units + rem
     A, B = inputs.make_operands(dtype, M, N, K, seed=500 + M)
     if dtype == "s8":
         assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
     else:
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+# Fewer tiles than the grid holds: every tile's k-blocks are spread over
+# several units (one tile over 128 units in the last case; the INT8 ranges
+# straddle the 1024-k accumulation chunks).
+SPLIT_SHAPES = [(256, 128, 8192), (100, 100, 65536), (512, 512, 4096), (300, 260, 5000), (129, 1000, 3000),
+                (1000, 40, 20000)]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_split_small_tile_counts(dev, dtype, M, N, K):
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    assert plan["split_tiles"] == plan["tiles"] and plan["units"] > plan["tiles"]
+    assert plan["units"] <= -(-plan["tiles"] * plan["k_blocks"] // 8)
+    A, B = inputs.make_operands(dtype, M, N, K, seed=900 + M + N + K)
+    if dtype == "s8":
+        assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+@pytest.mark.parametrize("pair", [1, 0], ids=["pair", "single"])
+def test_split_results_repeat_bit_for_bit(dev, pair):
+    # The parts of a split tile are added in a fixed order.
+    import torch
+    M, N, K = 1000, 700, 3000
+    A, B = inputs.make_operands("f16", M, N, K, seed=31)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, pair)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd)
+        assert plan["split_tiles"] > 0 and plan["cta_pair"] == pair
+        outs = []
+        for _ in range(3):
+            C = torch.empty((M, N), dtype=torch.float32, device=dev)
+            gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+            assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+            outs.append(C)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert_f16_close(outs[0].cpu().numpy(), oracle.gemm_f16f32(A, B))
+
+
+def test_split_plans_share_the_stream_workspace(dev):
+    # Split launches with different grids and tile widths take turns on one
+    # stream: the flags sit in a fixed region, never where another plan
+    # leaves its (small-integer INT8) partial sums.
+    import torch
+    shapes = [("s8", 1000, 700, 3000), ("f16", 256, 128, 8192), ("s8", 300, 100, 9000), ("f16", 1000, 40, 20000)]
+    ops = []
+    for dt, M, N, K in shapes:
+        A, B = inputs.make_operands(dt, M, N, K, seed=41 + M)
+        want = oracle.gemm_s8s8s32(A, B) if dt == "s8" else oracle.gemm_f16f32(A, B)
+        assert gemmpipe.gemmpipe_plan(0 if dt == "s8" else 1, M, N, K)["split_tiles"] > 0
+        C = torch.empty((M, N), dtype=torch.int32 if dt == "s8" else torch.float32, device=dev)
+        ops.append((dt, M, N, K, to_dev(A, dev), to_dev(B, dev), C, want))
+    for _ in range(8):
+        for dt, M, N, K, Ad, Bd, C, want in ops:
+            C.fill_(-1)
+            (gemmpipe.gemm_s8s8s32 if dt == "s8" else gemmpipe.gemm_f16f32)(M, N, K, Ad, Bd, C)
+            assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+            if dt == "s8":
+                assert np.array_equal(C.cpu().numpy(), want)
+            else:
+                assert_f16_close(C.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+def test_split_stall_times_out(dev, dtype):
+    # CTA 0 stalls on its first k-block: its own waits and the wait of the
+    # unit that adds its partial sums run out of time; nothing hangs, and
+    # the next call is correct.
+    import torch
+    M, N, K = 256, 128, 8192
+    A, B = inputs.make_operands(dtype, M, N, K, seed=37)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K, Ad, Bd)
+    assert plan["split_tiles"] == plan["tiles"]
+    out_t = torch.int32 if dtype == "s8" else torch.float32
+    C = torch.zeros((M, N), dtype=out_t, device=dev)
+    call = gemmpipe.gemm_s8s8s32 if dtype == "s8" else gemmpipe.gemm_f16f32
+    gemmpipe.gemmpipe_test_inject_stall(0, 200)
+    call(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+    call(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    if dtype == "s8":
+        assert np.array_equal(C.cpu().numpy(), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
 @pytest.mark.parametrize("dtype", ["f16", "s8"])
@@ -417,12 +509,13 @@ def test_cta_pair_stall_times_out(dev):
 
 
 def test_workload_fp16_4096_sampled(dev):
-    # The fp16 half of the headline metric: 4096^3, uniform [-1, 1]; 512
-    # tiles leave a last wave that runs as half-width tasks.
+    # The fp16 half of the headline metric: 4096^3, uniform [-1, 1]; the
+    # 256 pair tiles leave a partial last wave, so the last two waves are
+    # split into k-block ranges.
     M = N = K = 4096
     A, B = inputs.make_operands("f16", M, N, K, seed=inputs.SEED_BASE + 5)
     plan = gemmpipe.gemmpipe_plan(1, M, N, K)
-    assert plan["tasks"] >= plan["tiles"]
+    assert plan["tiles"] % plan["units"] == 0 or plan["split_tiles"] > 0
     got = run_f16(A, B, dev)
     rows = sample_rows(M)
     assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "fp16 4096^3")

@@ -1,0 +1,128 @@
+"""Host-side model of the persistent stream-K schedule, checked for the
+properties the kernel relies on (no GPU).
+
+The kernel walks each unit's items with the same rules: whole tiles
+round-robin, then the unit's equal share of the split k-blocks from its last
+tile back to its first.  A split tile's parts are added by the unit holding
+its last k-block, after waiting for the lower units holding its earlier
+k-blocks.  The model checks, over a sweep of tile counts, grid sizes and
+k-block counts, that
+
+* every k-block of every tile is computed exactly once;
+* a unit holds at most one part that ends inside a tile (one partial-sum
+  slot per unit), and it is that unit's first split item;
+* the unit adding a tile's parts waits only on lower units, each of which
+  publishes that part as its first split item (no cycle of waits, and with
+  CTAs dispatched in index order no wait on a CTA that cannot start);
+* no unit has an empty range.
+
+The grid choice mirrors the library's planner: tiles < slots splits all
+tiles over min(slots, ceil(tiles * k_blocks / 8)) units when that is more
+than the tile count; otherwise a partial last wave splits the last two
+waves' tiles (slots + tiles % slots) over all slots.
+"""
+from __future__ import annotations
+
+import itertools
+
+import pytest
+
+MIN_SPLIT_KB = 8
+
+
+def plan(tiles: int, slots: int, num_kb: int):
+    units, dp_tiles, sk_tiles = min(tiles, slots), tiles, 0
+    if tiles < slots:
+        u = min(slots, -(-tiles * num_kb // MIN_SPLIT_KB))
+        if u > tiles:
+            units, dp_tiles, sk_tiles = u, 0, tiles
+    elif tiles % slots and num_kb > 1:
+        sk_tiles = slots + tiles % slots
+        dp_tiles = tiles - sk_tiles
+    return units, dp_tiles, sk_tiles
+
+
+def sk_begin(sk_work: int, units: int, u: int) -> int:
+    return sk_work * u // units
+
+
+def items(u: int, units: int, dp_tiles: int, sk_tiles: int, num_kb: int):
+    """(tile, kb0, kb1, kind) in processing order; kinds as in the kernel."""
+    out = []
+    for t in range(u, dp_tiles, units):
+        out.append((t, 0, num_kb, 0))
+    sk_work = sk_tiles * num_kb
+    beg, pos = sk_begin(sk_work, units, u), sk_begin(sk_work, units, u + 1)
+    while pos > beg:
+        t = (pos - 1) // num_kb
+        ts = t * num_kb
+        kb1 = pos - ts
+        kb0 = beg - ts if beg > ts else 0
+        pos = ts + kb0
+        kind = 1 if kb1 < num_kb else (2 if kb0 > 0 else 0)
+        out.append((dp_tiles + t, kb0, kb1, kind))
+    return out
+
+
+def first_part_unit(u: int, sk_tile: int, units: int, sk_work: int, num_kb: int) -> int:
+    tile_start = sk_tile * num_kb
+    v = u - 1
+    while v > 0 and sk_begin(sk_work, units, v) > tile_start:
+        v -= 1
+    return v
+
+
+CASES = [(t, g, k) for t, g, k in itertools.product(
+    [1, 2, 3, 5, 17, 73, 74, 75, 100, 147, 148, 149, 160, 296, 300, 512],
+    [1, 2, 7, 74, 148],
+    [1, 2, 3, 7, 8, 9, 64, 65, 256])]
+
+
+@pytest.mark.parametrize("tiles,slots,num_kb", CASES)
+def test_schedule_properties(tiles, slots, num_kb):
+    units, dp_tiles, sk_tiles = plan(tiles, slots, num_kb)
+    assert units <= slots and dp_tiles + sk_tiles == tiles
+    sk_work = sk_tiles * num_kb
+    if sk_tiles:
+        assert sk_work >= units
+        for u in range(units):
+            assert sk_begin(sk_work, units, u + 1) > sk_begin(sk_work, units, u)
+    per_unit = [items(u, units, dp_tiles, sk_tiles, num_kb) for u in range(units)]
+    cover = {}
+    writers = {}  # tile -> units with a kind-1 part
+    for u, its in enumerate(per_unit):
+        kinds = [k for (_, _, _, k) in its]
+        assert kinds.count(1) <= 1
+        split = [it for it in its if it[0] >= dp_tiles]
+        if 1 in kinds:
+            assert split[0][3] == 1  # the first split item
+        if 2 in kinds:
+            assert its[-1][3] == 2 and kinds.count(2) == 1  # the last item
+        for (t, kb0, kb1, kind) in its:
+            assert 0 <= kb0 < kb1 <= num_kb
+            for kb in range(kb0, kb1):
+                assert (t, kb) not in cover
+                cover[(t, kb)] = u
+            if kind == 1:
+                writers.setdefault(t, []).append(u)
+    assert len(cover) == tiles * num_kb
+    finished = set()
+    for u, its in enumerate(per_unit):
+        for (t, kb0, kb1, kind) in its:
+            if kind == 2:
+                v_lo = first_part_unit(u, t - dp_tiles, units, sk_work, num_kb)
+                assert sorted(writers.get(t, [])) == list(range(v_lo, u))
+                finished.add(t)
+    # Every split tile that has writer parts is finished by exactly one unit.
+    assert set(writers) <= finished
+    for t in writers:
+        assert t >= dp_tiles
+
+
+def test_balance_when_tiles_overflow_the_grid():
+    # Equal shares: every unit's k-block count is within one tile's worth of
+    # the mean (whole tiles) plus one k-block (split ranges).
+    for tiles, slots, num_kb in [(256, 74, 64), (192, 74, 65), (512, 148, 64), (300, 148, 7)]:
+        units, dp, sk = plan(tiles, slots, num_kb)
+        work = [sum(kb1 - kb0 for (_, kb0, kb1, _) in items(u, units, dp, sk, num_kb)) for u in range(units)]
+        assert max(work) - min(work) <= 1
