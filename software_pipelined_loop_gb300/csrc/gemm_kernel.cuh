@@ -935,38 +935,55 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int h = e >> 2;                  // column half of the tile
     constexpr int NCOLS = Cfg::EPI_COLS;   // this warp's columns
+    constexpr int NB = NCOLS / 32;         // 32-column blocks
     constexpr bool INT = Cfg::INT_OUT;
+    constexpr bool ISUM = INT && !Cfg::SUM_IN_C;  // int32 running sums in registers
+    // HOLD (register-split variants, fp32 output): the warp copies its whole
+    // accumulator slice into registers and frees the TMEM buffer before any
+    // global traffic, so the MMA never waits on C stores or partial sums.
+    // Otherwise it works one 32-column block at a time.
+    constexpr bool HOLD = Cfg::REG_SPLIT && !INT;
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
     const int64_t me = unit_index<Cfg>();
     const int64_t my_slot = slot_of<Cfg>(me, rank);
     uint32_t acc = 0, acc_phase = 0;
+
+    auto release = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+            if constexpr (Cfg::PAIR)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));  // the leader's
+            else
+                mbar_arrive(smem_u32(&ctl->tempty[acc]));
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+    };
+    // The other parts of a split tile must be published before they are
+    // added.  Each is the first split item of a lower unit, which waits on
+    // nothing to produce it.
+    auto wait_parts = [&](int64_t v_lo) -> bool {
+        bool got = true;
+        for (int64_t v = me - 1; v >= v_lo && got; --v)
+            got = w.wait_flag(&p.flags[slot_of<Cfg>(v, rank) * Cfg::EPI_WARPS + e], p.epoch);
+        return __all_sync(0xffffffffu, got);
+    };
+
     WorkIter<Cfg> it(p);
     Work wk;
     while (it.next(p, wk)) {
         const int64_t row0 = wk.m0 + rank * Cfg::BM + q * 32;
         const int64_t colb = wk.n0 + h * NCOLS;
-        int64_t v_lo = me;
-        if (wk.kind == 2) {
-            // The other parts of this split tile must be published before
-            // they are added.  Each is the first split item of a lower unit,
-            // which waits on nothing to produce it.
-            v_lo = first_part_unit<Cfg>(p, wk.sk_tile);
-            bool got = true;
-            for (int64_t v = me - 1; v >= v_lo && got; --v)
-                got = w.wait_flag(&p.flags[slot_of<Cfg>(v, rank) * Cfg::EPI_WARPS + e], p.epoch);
-            if (!__all_sync(0xffffffffu, got)) return;
-        }
-        uint32_t isum[(INT && !Cfg::SUM_IN_C) ? NCOLS : 1];
-        if constexpr (INT && !Cfg::SUM_IN_C) {
-            // Integer sums: the other parts of a split tile can start them
-            // (the order of exact additions does not matter).
+        const int64_t v_lo = wk.kind == 2 ? first_part_unit<Cfg>(p, wk.sk_tile) : me;
+        if (!HOLD && !ISUM && wk.kind == 2 && !wait_parts(v_lo)) return;
+        uint32_t val[(HOLD || ISUM) ? NCOLS : 1];  // fp32 bits (HOLD) or int32 sums (ISUM)
+        if constexpr (ISUM) {
 #pragma unroll
-            for (int i = 0; i < NCOLS; ++i) isum[i] = 0;
-            for (int64_t v = me - 1; v >= v_lo; --v)
-#pragma unroll
-                for (int jb = 0; jb < NCOLS / 32; ++jb)
-                    add_part<true>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), &isum[jb * 32], lane);
+            for (int i = 0; i < NCOLS; ++i) val[i] = 0;
         }
+        // fp32 output: one accumulation per item (the chunk is the whole
+        // k-range); INT8: one per chunk of at most 1024 k values.
         for (int64_t kc = wk.kb0; kc < wk.kb1; kc += p.kb_per_chunk) {
             const bool got = w.wait(smem_u32(&ctl->tfull[acc]), acc_phase);
             if (!__all_sync(0xffffffffu, got)) return;
@@ -977,7 +994,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
                 // first chunk stores them, later chunks add into C (each
                 // element is read and written by the same thread, in order).
 #pragma unroll
-                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                for (int jb = 0; jb < NB; ++jb) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + jb * 32, r);
                     tmem_wait_ld();
@@ -988,21 +1005,26 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
                     else
                         store_block<true>(p, stg, r, row0, colb + jb * 32, lane);
                 }
-            } else if constexpr (INT) {
+            } else if constexpr (ISUM) {
                 // Chunk partials are integers below 2^24 in magnitude: exact
                 // in fp32, so the conversion is exact.
 #pragma unroll
-                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                for (int jb = 0; jb < NB; ++jb) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + jb * 32, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        isum[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
+                        val[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
                 }
+            } else if constexpr (HOLD) {
+#pragma unroll
+                for (int jb = 0; jb < NB; ++jb)
+                    tmem_ld_32x32b_x32(tbase + jb * 32, *reinterpret_cast<uint32_t(*)[32]>(&val[jb * 32]));
+                tmem_wait_ld();
             } else {
 #pragma unroll
-                for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                for (int jb = 0; jb < NB; ++jb) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + jb * 32, r);
                     tmem_wait_ld();
@@ -1015,24 +1037,25 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (Cfg::PAIR)
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));  // the leader's
-                else
-                    mbar_arrive(smem_u32(&ctl->tempty[acc]));
-            }
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            release();
         }
-        if constexpr (INT && !Cfg::SUM_IN_C) {
+        if constexpr (ISUM || HOLD) {
+            // The accumulator is already free.  A split tile's other parts
+            // are added in unit order (exact for integers; a fixed order for
+            // fp32), then the slice goes to C or to this unit's slot.
+            if (wk.kind == 2) {
+                if (!wait_parts(v_lo)) return;
+                for (int64_t v = me - 1; v >= v_lo; --v)
 #pragma unroll
-            for (int jb = 0; jb < NCOLS / 32; ++jb) {
+                    for (int jb = 0; jb < NB; ++jb)
+                        add_part<INT>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), &val[jb * 32], lane);
+            }
+#pragma unroll
+            for (int jb = 0; jb < NB; ++jb) {
                 if (wk.kind == 1)
-                    write_part(part_block<Cfg>(p, my_slot, e, jb), &isum[jb * 32], lane);
+                    write_part(part_block<Cfg>(p, my_slot, e, jb), &val[jb * 32], lane);
                 else
-                    store_block(p, stg, &isum[jb * 32], row0, colb + jb * 32, lane);
+                    store_block(p, stg, &val[jb * 32], row0, colb + jb * 32, lane);
             }
         }
         if (wk.kind == 1) {
