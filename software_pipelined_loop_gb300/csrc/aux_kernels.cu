@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <utility>
 
 #include "ptx.cuh"
 #include "variants.h"
@@ -80,26 +81,151 @@ __device__ __forceinline__ void widen_store(const WidenJob &j, int64_t r, int64_
 }
 
 // blockIdx.z picks the matrix (0: A, 1: B); x covers 16-element pieces of a
-// row, y strides over rows.  Four rows' loads are issued before any of them
-// is widened and stored, so each thread keeps four loads in flight.
+// row, y strides over rows.  Each thread issues the loads of up to kRowBatch
+// rows (its last batch predicated) before widening and storing any of them,
+// so a thread's rows cost one memory round trip per batch.
+constexpr int kRowBatch = 8;
+
 __global__ void widen_s8_f16_kernel(const WidenJob ja, const WidenJob jb)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const WidenJob &j = blockIdx.z == 0 ? ja : jb;
     const int64_t c = 16 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
     if (c >= j.pitch) return;
     const int64_t step = gridDim.y;
-    int64_t r = blockIdx.y;
-    for (; r + 3 * step < j.rows; r += 4 * step) {
-        const uint4 v0 = widen_load(j, r, c);
-        const uint4 v1 = widen_load(j, r + step, c);
-        const uint4 v2 = widen_load(j, r + 2 * step, c);
-        const uint4 v3 = widen_load(j, r + 3 * step, c);
-        widen_store(j, r, c, v0);
-        widen_store(j, r + step, c, v1);
-        widen_store(j, r + 2 * step, c, v2);
-        widen_store(j, r + 3 * step, c, v3);
+    for (int64_t r = blockIdx.y; r < j.rows; r += kRowBatch * step) {
+        uint4 v[kRowBatch];
+#pragma unroll
+        for (int i = 0; i < kRowBatch; ++i)
+            if (r + i * step < j.rows) v[i] = widen_load(j, r + i * step, c);
+#pragma unroll
+        for (int i = 0; i < kRowBatch; ++i)
+            if (r + i * step < j.rows) widen_store(j, r + i * step, c, v[i]);
     }
-    for (; r < j.rows; r += step) widen_store(j, r, c, widen_load(j, r, c));
+}
+
+// Widening of operands whose rows are whole 16-byte units (cols a multiple
+// of 16, 16-byte aligned bases, destination pitch == cols): each matrix is
+// one contiguous array of n int8 (n a multiple of 16) and becomes n fp16.
+// One CTA per SM streams 16 KiB chunks: a bulk copy brings a chunk into one
+// of kFlatInStages shared-memory stages (completion on the stage's
+// mbarrier), the threads widen it into one of kFlatOut output buffers, and
+// a bulk copy writes that to global memory.  Loads run kFlatInStages chunks
+// ahead; one CTA barrier per chunk orders the widening before the store.
+struct FlatJob {
+    const int8_t *src;
+    uint16_t *dst;
+    int64_t n;
+};
+
+constexpr int kFlatChunk = 16384;  // int8 bytes per chunk
+constexpr int kFlatInStages = 6;
+constexpr int kFlatOut = 3;
+constexpr int kFlatThreads = 256;
+constexpr int kFlatSmem = kFlatInStages * kFlatChunk + kFlatOut * 2 * kFlatChunk + 8 * kFlatInStages + 128;
+static_assert(kFlatOut >= 3, "an output buffer is rewritten two chunks after its store was confirmed read");
+static_assert(kFlatSmem <= 232448, "over the per-CTA shared-memory limit");
+
+__global__ void __launch_bounds__(kFlatThreads, 1)
+    widen_flat_kernel(const FlatJob ja, const FlatJob jb, int *status, uint64_t timeout_ns)
+{
+    extern __shared__ __align__(128) uint8_t fsm[];
+    const uint32_t base = (smem_u32(fsm) + 127u) & ~127u;
+    const uint32_t in0 = base;
+    const uint32_t out0 = base + kFlatInStages * kFlatChunk;
+    const uint32_t bar0 = out0 + kFlatOut * 2 * kFlatChunk;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t ca = (ja.n + kFlatChunk - 1) / kFlatChunk;
+    const int64_t total = ca + (jb.n + kFlatChunk - 1) / kFlatChunk;
+    const int64_t mine = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    // Source, destination and size of this CTA's i-th chunk.
+    auto chunk = [&](int64_t i, const int8_t *&src, uint16_t *&dst, uint32_t &bytes) {
+        const int64_t g = blockIdx.x + i * gridDim.x;
+        const FlatJob &j = g < ca ? ja : jb;
+        const int64_t off = (g < ca ? g : g - ca) * kFlatChunk;
+        const int64_t left = j.n - off;
+        bytes = static_cast<uint32_t>(left < kFlatChunk ? left : kFlatChunk);
+        src = j.src + off;
+        dst = j.dst + off;
+    };
+    auto issue = [&](int64_t i) {
+        const int8_t *src;
+        uint16_t *dst;
+        uint32_t bytes;
+        chunk(i, src, dst, bytes);
+        const int st = static_cast<int>(i % kFlatInStages);
+        mbar_arrive_expect_tx(bar0 + 8 * st, bytes);
+        bulk_load_g2s(in0 + st * kFlatChunk, src, bytes, bar0 + 8 * st);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kFlatInStages; ++st) mbar_init(bar0 + 8 * st, 1);
+        fence_mbar_init();
+        for (int64_t i = 0; i < mine && i < kFlatInStages; ++i) issue(i);
+    }
+    __syncthreads();
+    int64_t issued = mine < kFlatInStages ? mine : kFlatInStages;
+    int64_t i = 0;
+    for (; i < mine; ++i) {
+        const int st = static_cast<int>(i % kFlatInStages);
+        const uint32_t parity = static_cast<uint32_t>((i / kFlatInStages) & 1);
+        const uint32_t ob = out0 + static_cast<uint32_t>(i % kFlatOut) * (2 * kFlatChunk);
+        bool late = false;
+        if (!mbar_try_wait(bar0 + 8 * st, parity)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar0 + 8 * st, parity))
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    late = true;
+                    break;
+                }
+        }
+        const int8_t *src;
+        uint16_t *dst;
+        uint32_t bytes;
+        chunk(i, src, dst, bytes);
+        if (!late) {
+            // 8 int8 -> 8 fp16 per step; a warp reads 256 and writes 512
+            // contiguous bytes.
+            const uint32_t ib = in0 + st * kFlatChunk;
+            for (uint32_t b = 8 * threadIdx.x; b < bytes; b += 8 * kFlatThreads) {
+                const uint2 v = ld_shared_v2(ib + b);
+                uint32_t o0, o1, o2, o3;
+                widen4(v.x, o0, o1);
+                widen4(v.y, o2, o3);
+                st_shared_v4(ob + 2 * b, o0, o1, o2, o3);
+            }
+            fence_proxy_async_smem();
+        }
+        if (__syncthreads_or(late)) break;
+        if (threadIdx.x == 0) {
+            bulk_store_s2g(dst, ob, 2 * bytes);
+            bulk_commit();
+            if (issued < mine) {
+                issue(issued);  // into stage st, just consumed
+                ++issued;
+            }
+            // The output buffer of chunk i + 2 was last read by the store of
+            // chunk i - 1: done once at most one group (chunk i) is reading.
+            bulk_wait_read<1>();
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (i < mine) {
+            // A load ran out of time: record it, and let every load still
+            // in flight land before the CTA's shared memory goes away.
+            atomicCAS(status, 0, static_cast<int>(GEMMPIPE_ERR_TIMEOUT));
+            for (int64_t k = i; k < issued; ++k) {
+                const int st = static_cast<int>(k % kFlatInStages);
+                const uint32_t parity = static_cast<uint32_t>((k / kFlatInStages) & 1);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar0 + 8 * st, parity))
+                    if (globaltimer_ns() - t0 > timeout_ns) break;
+            }
+        }
+        bulk_wait<0>();
+    }
+    __syncthreads();
 }
 
 // Copies a rows x cols fp16 matrix (densely packed, any 2-byte alignment)
@@ -150,31 +276,32 @@ __device__ __forceinline__ void pad_store(const PadJob &j, int64_t r, int64_t c,
     *reinterpret_cast<uint4 *>(j.dst + r * j.pitch + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// x covers 8-element pieces of a row, y strides over rows with four rows'
-// loads in flight per thread; z picks one of two jobs (A and B padded in
-// one launch).
+// x covers 8-element pieces of a row, y strides over rows in batches of
+// kRowBatch rows whose loads are all in flight together; z picks one of two
+// jobs (A and B padded in one launch).
 __global__ void pad_f16_kernel(const PadJob j0, const PadJob j1)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const PadJob &j = blockIdx.z == 0 ? j0 : j1;
     const int64_t c = 8 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
     if (c >= j.pitch) return;
     const int64_t step = gridDim.y;
-    int64_t r = blockIdx.y;
-    for (; r + 3 * step < j.rows; r += 4 * step) {
-        const PadLoad l0 = pad_load(j, r, c);
-        const PadLoad l1 = pad_load(j, r + step, c);
-        const PadLoad l2 = pad_load(j, r + 2 * step, c);
-        const PadLoad l3 = pad_load(j, r + 3 * step, c);
-        pad_store(j, r, c, l0);
-        pad_store(j, r + step, c, l1);
-        pad_store(j, r + 2 * step, c, l2);
-        pad_store(j, r + 3 * step, c, l3);
+    for (int64_t r = blockIdx.y; r < j.rows; r += kRowBatch * step) {
+        PadLoad l[kRowBatch];
+#pragma unroll
+        for (int i = 0; i < kRowBatch; ++i)
+            if (r + i * step < j.rows) l[i] = pad_load(j, r + i * step, c);
+#pragma unroll
+        for (int i = 0; i < kRowBatch; ++i)
+            if (r + i * step < j.rows) pad_store(j, r + i * step, c, l[i]);
     }
-    for (; r < j.rows; r += step) pad_store(j, r, c, pad_load(j, r, c));
 }
 
 __global__ void zero_fill_kernel(uint8_t *dst, int64_t bytes)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const uintptr_t addr = reinterpret_cast<uintptr_t>(dst);
@@ -189,6 +316,8 @@ __global__ void zero_fill_kernel(uint8_t *dst, int64_t bytes)
 
 __global__ void copy_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0) {
@@ -202,25 +331,97 @@ __global__ void copy_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes)
     }
 }
 
+// Launches with programmatic dependent launch allowed: every kernel here
+// starts with pdl_wait, so it may be scheduled while the previous grid on
+// the stream finishes.
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*k)(P...), dim3 grid, int threads, cudaStream_t s, A &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k, std::forward<A>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+// Blocks of `threads` threads of kernel k resident on one SM (cached per
+// kernel; 8 if the query fails).
+template <class K>
+int resident_blocks(K k, int threads)
+{
+    static std::atomic<int> cached{0};
+    int n = cached.load();
+    if (n > 0) return n;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, 0) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 8;
+    }
+    cached.store(n);
+    return n;
+}
+
 cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16, int64_t pitchA,
                                 const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB,
                                 int sms, cudaStream_t s)
 {
+    const auto flat = [](const void *src, const void *dst, int64_t cols, int64_t pitch) {
+        return cols % 16 == 0 && pitch == cols && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
+               (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+    };
+    if (flat(A, A16, colsA, pitchA) && flat(B, B16, colsB, pitchB)) {
+        static std::atomic<int> attr_done[128];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+        if (!attr_done[dev].load()) {
+            e = cudaFuncSetAttribute(widen_flat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFlatSmem);
+            if (e != cudaSuccess) return e;
+            attr_done[dev].store(1);
+        }
+        int *st = nullptr;
+        if ((e = status_word(&st)) != cudaSuccess) return e;
+        const FlatJob fa{A, A16, rowsA * colsA};
+        const FlatJob fb{B, B16, rowsB * colsB};
+        const int64_t chunks = (fa.n + kFlatChunk - 1) / kFlatChunk + (fb.n + kFlatChunk - 1) / kFlatChunk;
+        const int grid = static_cast<int>(chunks < sms ? chunks : sms);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid > 0 ? grid : 1, 1, 1);
+        cfg.blockDim = dim3(kFlatThreads, 1, 1);
+        cfg.dynamicSmemBytes = kFlatSmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, widen_flat_kernel, fa, fb, st, static_cast<uint64_t>(2000000000ull));
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const WidenJob ja{A, rowsA, colsA, A16, pitchA};
     const WidenJob jb{B, rowsB, colsB, B16, pitchB};
     const int threads = 128;
     const int64_t maxpitch = pitchA > pitchB ? pitchA : pitchB;
     const int64_t gx = ((maxpitch + 15) / 16 + threads - 1) / threads;
     const int64_t maxrows = rowsA > rowsB ? rowsA : rowsB;
-    // About eight blocks of 128 threads per SM for each matrix.
-    int64_t gy = (static_cast<int64_t>(sms) * 8 + gx - 1) / gx;
-    // Prefer whole groups of four rows per y-block.
-    if (gy * 4 > maxrows) gy = (maxrows + 3) / 4;
+    // One resident wave of blocks over both matrices, and at least a whole
+    // batch of rows per thread.
+    const int64_t wave = static_cast<int64_t>(sms) * resident_blocks(widen_s8_f16_kernel, threads);
+    int64_t gy = (wave / 2 + gx - 1) / gx;
+    if (gy * kRowBatch > maxrows) gy = (maxrows + kRowBatch - 1) / kRowBatch;
     gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
     gy = gy > 65535 ? 65535 : gy;
     if (gx > 2147483647) return cudaErrorInvalidValue;
-    widen_s8_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2), threads, 0, s>>>(ja, jb);
-    return cudaGetLastError();
+    return launch_pdl(widen_s8_f16_kernel, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 2), threads, s,
+                      ja, jb);
 }
 
 cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
@@ -234,14 +435,15 @@ cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, u
     const int64_t maxpitch = pitch0 > pitch1 ? pitch0 : pitch1;
     const int64_t maxrows = rows0 > rows1 ? rows0 : rows1;
     const int64_t gx = (maxpitch / 8 + threads - 1) / threads;
-    int64_t gy = (static_cast<int64_t>(sms) * 16 + gx - 1) / gx;
-    if (gy * 4 > maxrows) gy = (maxrows + 3) / 4;
+    const unsigned gz = rows1 > 0 ? 2u : 1u;
+    const int64_t wave = static_cast<int64_t>(sms) * resident_blocks(pad_f16_kernel, threads);
+    int64_t gy = (wave / gz + gx - 1) / gx;
+    if (gy * kRowBatch > maxrows) gy = (maxrows + kRowBatch - 1) / kRowBatch;
     gy = gy < 1 ? 1 : (gy > maxrows ? maxrows : gy);
     gy = gy > 65535 ? 65535 : gy;
     if (gx > 2147483647) return cudaErrorInvalidValue;
-    const unsigned gz = rows1 > 0 ? 2u : 1u;
-    pad_f16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), gz), threads, 0, s>>>(j0, j1);
-    return cudaGetLastError();
+    return launch_pdl(pad_f16_kernel, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), gz), threads, s, j0,
+                      j1);
 }
 
 cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s)
@@ -249,8 +451,7 @@ cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s)
     const int64_t need = (bytes / 16 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sms) * 4;
     const int grid = static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
-    zero_fill_kernel<<<grid, 256, 0, s>>>(static_cast<uint8_t *>(dst), bytes);
-    return cudaGetLastError();
+    return launch_pdl(zero_fill_kernel, dim3(grid), 256, s, static_cast<uint8_t *>(dst), bytes);
 }
 
 cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s)
@@ -258,8 +459,8 @@ cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cuda
     const int64_t need = (bytes / 16 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     const int grid = static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
-    copy_kernel<<<grid, 256, 0, s>>>(static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), bytes);
-    return cudaGetLastError();
+    return launch_pdl(copy_kernel, dim3(grid), 256, s, static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src),
+                      bytes);
 }
 
 cudaError_t status_word(int **ptr)

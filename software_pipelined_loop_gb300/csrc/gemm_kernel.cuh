@@ -1120,6 +1120,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if constexpr (Cfg::PAIR) cluster_sync();  // the leader's barriers exist before the peer signals them
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
+    // The set-up above touches no global memory, so it overlaps the end of
+    // the previous grid on the stream; from here on its results are visible.
+    pdl_wait();
+    pdl_launch_dependents();
     const Waiter w{&ctl->abort, p.status, p.timeout_ns};
     const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
     if constexpr (Cfg::REG_SPLIT) {

@@ -155,6 +155,11 @@ constexpr int64_t kSplitFlagBytes = kMaxSplitCtas * kSplitFlagsPerCta * 4;
 // SMs they replace.
 constexpr int64_t kMinSplitKb = 8;
 
+// Dense fp16 tensor flops per byte of HBM traffic at which GB300 turns from
+// memory- to compute-bound (about 2.2 PFLOP/s over 7.9 TB/s; a copy and a
+// cuBLAS GEMM measure 1.9 PFLOP/s over 6.8 TB/s, the same ratio).
+constexpr double kMachineBalance = 280.0;
+
 int64_t Plan::split_bytes() const
 {
     if (sk_tiles == 0) return 0;
@@ -238,15 +243,23 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     const bool split = split_ok && v->info.split_ok && ov.split != 0;
     pl->slots = slots;
     pl->run_whole_tiles();
+    // A memory-bound GEMM (flops per compulsory byte below the machine
+    // balance) whose tiles already occupy half the SMs or more gains
+    // nothing from more SMs, only the fix-up traffic: its tiles stay whole.
+    const double flops = 2.0 * static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+    const double esz_in = convert ? 1.0 : 2.0;  // operand bytes the kernel reads
+    const double bytes =
+        esz_in * (static_cast<double>(M) * K + static_cast<double>(K) * N) + 4.0 * static_cast<double>(M) * N;
+    const bool memory_bound = flops < kMachineBalance * bytes;
     if (split && T < slots) {
         const int64_t want = (T * pl->num_kb + kMinSplitKb - 1) / kMinSplitKb;
         const int64_t u = want < slots ? want : slots;
-        if (u > T) {
+        if (u > T && !(memory_bound && 2 * T >= slots)) {
             pl->units = u;
             pl->dp_tiles = 0;
             pl->sk_tiles = T;
         }
-    } else if (split && T % slots != 0 && pl->num_kb > 1) {
+    } else if (split && T > slots && T % slots != 0 && pl->num_kb > 1) {
         pl->sk_tiles = slots + T % slots;
         pl->dp_tiles = T - pl->sk_tiles;
     }

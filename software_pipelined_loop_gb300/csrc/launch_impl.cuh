@@ -32,26 +32,28 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmPar
         }
         attr_done[dev].store(1);
     }
+    // Programmatic dependent launch: the CTAs may start (and run the set-up
+    // that reads no global memory) while the previous grid finishes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (Cfg::PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemm_pipelined_kernel<Cfg>, a, b, p);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
-    } else {
-        gemm_pipelined_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p);
-        return cudaGetLastError();
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
+    e = cudaLaunchKernelEx(&cfg, gemm_pipelined_kernel<Cfg>, a, b, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 // Number of CTA pairs of this variant the current device can hold at once
