@@ -414,8 +414,10 @@ def run_gpu(args) -> int:
         val = r["bytes_per_s"] if r["N"] <= 128 else r["ops_per_s"]
         return {"value": val, "unit": unit, "ms_per_step": r["ms"], "kernel_ms": r["kernel_ms"],
                 "roofline": r["roofline"], "l2": r["l2"],
-                "plan": {k: r["plan"][k] for k in ("producer", "BN", "stages", "grid", "tiles", "split_tiles")},
-                "shape": [r["M"], r["N"], r["K"]]}
+                "plan": {k: r["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair",
+                                                   "grid", "units", "tiles", "split_tiles", "k_blocks",
+                                                   "smem_bytes", "operand_copy")},
+                "shape": [r["M"], r["N"], r["K"]], "dtype": r["dtype"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -428,8 +430,9 @@ def run_gpu(args) -> int:
         "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
                    "l2": head["l2"] + " (between timed steps: 256 MiB written, then another 256 MiB read, "
                                       "when inputs < L2)",
-                   "plan": {k: head["plan"][k] for k in ("producer", "BN", "stages", "threads", "grid", "units", "split_tiles",
-                                                         "operand_copy")},
+                   "plan": {k: head["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair",
+                                                         "grid", "units", "tiles", "split_tiles", "k_blocks",
+                                                         "smem_bytes", "operand_copy")},
                    "replicas": world},
         "roofline": head["roofline"],
         "cpu_baseline": cpu,
