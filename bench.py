@@ -462,7 +462,9 @@ ABLATION = [
     # (label, dtype, shape, producer, bn, stages, cta_pair, split)
     ("pair S=1 (load, wait, compute)", "f16", SQUARE, 0, 256, 1, 1, -1),
     ("pair S=2 (double buffer)", "f16", SQUARE, 0, 256, 2, 1, -1),
+    ("pair S=3", "f16", SQUARE, 0, 256, 3, 1, -1),
     ("pair S=4", "f16", SQUARE, 0, 256, 4, 1, -1),
+    ("pair S=5", "f16", SQUARE, 0, 256, 5, 1, -1),
     ("pair S=6 (default)", "f16", SQUARE, 0, 256, 6, 1, -1),
     ("pair S=6, every tile whole (no stream-K)", "f16", SQUARE, 0, 256, 6, 1, 0),
     ("single CTA 128x256 S=4", "f16", SQUARE, 0, 256, 4, 0, -1),
@@ -474,8 +476,9 @@ ABLATION = [
     ("int8: in-kernel widening, single CTA", "s8", SQUARE, 0, 256, 2, 0, -1),
     ("ragged fp16: stream-K (default)", "f16", RAGGED, -1, 0, 0, -1, -1),
     ("ragged fp16: every tile whole", "f16", RAGGED, -1, 0, 0, -1, 0),
-    ("skinny fp16: stream-K (default)", "f16", SKINNY, -1, 0, 0, -1, -1),
-    ("skinny fp16: every tile whole", "f16", SKINNY, -1, 0, 0, -1, 0),
+    ("skinny fp16: TMA producer (default)", "f16", SKINNY, -1, 0, 0, -1, -1),
+    ("skinny fp16: stream-K forced on all 152 SMs", "f16", SKINNY, -1, 0, 0, -1, 1),
+    ("skinny fp16: bounded-load producer", "f16", SKINNY, 1, 128, 6, 0, -1),
 ]
 
 

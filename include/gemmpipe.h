@@ -244,8 +244,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * ring depths (when the chosen variant has no such depth the automatic one
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
  * 0 single CTAs, 1 CTA pairs where the shape allows them.  split: -1
- * automatic, 0 every tile whole (no stream-K split).  Returns
- * INVALID_VALUE for values outside these sets.
+ * automatic, 0 every tile whole (no stream-K split), 1 split wherever the
+ * schedule can (also memory-bound shapes whose tiles already fill half the
+ * grid).  Returns INVALID_VALUE for values outside these sets.
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair,
                                                           int split);

@@ -7,10 +7,12 @@ static const Variant kF16Variants[] = {
     make_variant<GemmCfg<256, 4, false, false>>(),  // TMA producer, 128x256 tiles
     make_variant<GemmCfg<256, 6, false, false, false, 1, true>>(),  // CTA pair, 256x256 tiles
     // Ring-depth ablation: 1 = load, wait, compute (no overlap); 2 = the
-    // classic double buffer; 4.
+    // classic double buffer; 3 to 5.
     make_variant<GemmCfg<256, 1, false, false, false, 1, true>>(),
     make_variant<GemmCfg<256, 2, false, false, false, 1, true>>(),
+    make_variant<GemmCfg<256, 3, false, false, false, 1, true>>(),
     make_variant<GemmCfg<256, 4, false, false, false, 1, true>>(),
+    make_variant<GemmCfg<256, 5, false, false, false, 1, true>>(),
     make_variant<GemmCfg<128, 6, false, false>>(),  // TMA producer, 128x128 tiles (N <= 128)
     make_variant<GemmCfg<256, 4, true, false>>(),   // bounded-load producer (misaligned inputs)
     make_variant<GemmCfg<128, 6, true, false>>(),

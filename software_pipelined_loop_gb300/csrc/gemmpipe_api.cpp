@@ -254,7 +254,7 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (split && T < slots) {
         const int64_t want = (T * pl->num_kb + kMinSplitKb - 1) / kMinSplitKb;
         const int64_t u = want < slots ? want : slots;
-        if (u > T && !(memory_bound && 2 * T >= slots)) {
+        if (u > T && (ov.split == 1 || !(memory_bound && 2 * T >= slots))) {
             pl->units = u;
             pl->dp_tiles = 0;
             pl->sk_tiles = T;
@@ -808,7 +808,7 @@ gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, i
     if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
     if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;
-    if (split < -1 || split > 0) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (split < -1 || split > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_override.producer = producer;
     g_override.bn = bn;

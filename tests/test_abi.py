@@ -72,7 +72,7 @@ def test_host_side_argument_checks(lib):
     assert lib.gemmpipe_set_plan_override(2, 0, 0, -1, -1) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 192, 0, -1, -1) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 0, 0, 2, -1) == gemmpipe.ERR_INVALID_VALUE
-    assert lib.gemmpipe_set_plan_override(-1, 0, 0, -1, 1) == gemmpipe.ERR_INVALID_VALUE
+    assert lib.gemmpipe_set_plan_override(-1, 0, 0, -1, 2) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 0, 0, -1, -1) == gemmpipe.OK
     assert lib.gemmpipe_test_inject_stall(3, 0) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_test_inject_stall(-1, 0) == gemmpipe.OK

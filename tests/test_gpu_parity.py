@@ -420,6 +420,25 @@ def test_split_results_repeat_bit_for_bit(dev, pair):
     assert_f16_close(outs[0].cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
+def test_memory_bound_half_full_grid_keeps_whole_tiles(dev):
+    # 100 tiles of 128 x 128 over 152 SMs, 113 flops per byte (memory-bound):
+    # whole tiles by default; the split override still splits, same result.
+    M, N, K = 12800, 128, 2048
+    A, B = inputs.make_operands("f16", M, N, K, seed=43)
+    want = oracle.gemm_f16f32(A, B)
+    plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+    assert plan["tiles"] == 100 and plan["split_tiles"] == 0 and plan["units"] == 100
+    assert_f16_close(run_f16(A, B, dev), want)
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, 1)
+    try:
+        forced = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert forced["split_tiles"] == 100 and forced["units"] > 100
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert_f16_close(got, want)
+
+
 def test_split_plans_share_the_stream_workspace(dev):
     # Split launches with different grids and tile widths take turns on one
     # stream: the flags sit in a fixed region, never where another plan
@@ -556,7 +575,7 @@ def test_s8_stall_times_out_in_converter_variant(dev):
     assert np.array_equal(C.cpu().numpy(), oracle.gemm_s8s8s32(A, B))
 
 
-@pytest.mark.parametrize("stages", [1, 2, 4, 6])
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5, 6])
 def test_ring_depths_of_cta_pair(dev, stages):
     # S = 1: the producer waits for the MMAs to release the only stage
     # before every load (load, wait, compute -- no overlap); S = 2: the
