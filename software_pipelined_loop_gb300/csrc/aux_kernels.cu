@@ -125,6 +125,9 @@ constexpr int kFlatOut = 3;
 constexpr int kFlatThreads = 256;
 constexpr int kFlatSmem = kFlatInStages * kFlatChunk + kFlatOut * 2 * kFlatChunk + 8 * kFlatInStages + 128;
 static_assert(kFlatOut >= 3, "an output buffer is rewritten two chunks after its store was confirmed read");
+// Bulk stores allowed to still read shared memory at the end of an
+// iteration: the buffer of chunk i + 2 was last read by the store of chunk
+// i + 2 - kFlatOut, which is then finished.
 static_assert(kFlatSmem <= 232448, "over the per-CTA shared-memory limit");
 
 __global__ void __launch_bounds__(kFlatThreads, 1)
@@ -206,8 +209,9 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
                 ++issued;
             }
             // The output buffer of chunk i + 2 was last read by the store of
-            // chunk i - 1: done once at most one group (chunk i) is reading.
-            bulk_wait_read<1>();
+            // chunk i + 2 - kFlatOut: done once at most kFlatOut - 2 groups
+            // (the newest stores) are still reading.
+            bulk_wait_read<kFlatOut - 2>();
         }
     }
     if (threadIdx.x == 0) {
@@ -296,6 +300,166 @@ __global__ void pad_f16_kernel(const PadJob j0, const PadJob j1)
         for (int i = 0; i < kRowBatch; ++i)
             if (r + i * step < j.rows) pad_store(j, r + i * step, c, l[i]);
     }
+}
+
+// The same copy with bulk copies, for rows that fit a shared-memory stage:
+// a chunk of whole source rows is fetched as the 16-byte granules that hold
+// it (the granules contain bytes of the rows, so the fetch stays in the
+// allocation's pages), realigned row by row into an output buffer whose
+// rows have the destination pitch (slots past `cols` zero), and written
+// back with one bulk store.  Same pipeline shape as widen_flat_kernel.
+struct RowsJob {
+    const uint16_t *src;
+    int64_t rows, cols;
+    uint16_t *dst;
+    int64_t pitch;
+    int64_t rows_per_chunk;  // whole rows per chunk, >= 1
+};
+
+constexpr int kRowsCap = 32768;  // bytes per input stage and per output buffer
+constexpr int kRowsInStages = 4;
+constexpr int kRowsOut = 3;
+constexpr int kRowsThreads = 512;
+constexpr int kRowsSmem = kRowsInStages * kRowsCap + kRowsOut * kRowsCap + 8 * kRowsInStages + 128;
+static_assert(kRowsSmem <= 232448, "over the per-CTA shared-memory limit");
+static_assert(kRowsOut >= 3, "an output buffer is rewritten two chunks after its store was confirmed read");
+
+struct RowsChunk {
+    uintptr_t load;     // 16-byte aligned start of the fetched granules
+    uint32_t in_bytes;  // fetched bytes (a multiple of 16)
+    uint32_t shift;     // byte offset of the chunk's first element in them
+    int64_t rows;       // rows in the chunk
+    uint16_t *dst;
+    uint32_t out_bytes;
+};
+
+__device__ __forceinline__ RowsChunk rows_chunk(const RowsJob &j, int64_t k)
+{
+    RowsChunk c;
+    const int64_t r0 = k * j.rows_per_chunk;
+    const int64_t r1 = r0 + j.rows_per_chunk < j.rows ? r0 + j.rows_per_chunk : j.rows;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(j.src + r0 * j.cols);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(j.src + r1 * j.cols);
+    c.load = a0 & ~static_cast<uintptr_t>(15);
+    c.in_bytes = static_cast<uint32_t>(((a1 + 15) & ~static_cast<uintptr_t>(15)) - c.load);
+    c.shift = static_cast<uint32_t>(a0 - c.load);
+    c.rows = r1 - r0;
+    c.dst = j.dst + r0 * j.pitch;
+    c.out_bytes = static_cast<uint32_t>(c.rows * j.pitch * 2);
+    return c;
+}
+
+__global__ void __launch_bounds__(kRowsThreads, 1)
+    pad_rows_kernel(const RowsJob j0, const RowsJob j1, int *status, uint64_t timeout_ns)
+{
+    extern __shared__ __align__(128) uint8_t rsm[];
+    const uint32_t base = (smem_u32(rsm) + 127u) & ~127u;
+    const uint32_t in0 = base;
+    const uint32_t out0 = base + kRowsInStages * kRowsCap;
+    const uint32_t bar0 = out0 + kRowsOut * kRowsCap;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t c0 = (j0.rows + j0.rows_per_chunk - 1) / j0.rows_per_chunk;
+    const int64_t total = c0 + (j1.rows > 0 ? (j1.rows + j1.rows_per_chunk - 1) / j1.rows_per_chunk : 0);
+    const int64_t mine = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto job_of = [&](int64_t i, int64_t &k) -> const RowsJob & {
+        const int64_t g = blockIdx.x + i * gridDim.x;
+        k = g < c0 ? g : g - c0;
+        return g < c0 ? j0 : j1;
+    };
+    auto issue = [&](int64_t i) {
+        int64_t k;
+        const RowsChunk c = rows_chunk(job_of(i, k), k);
+        const int st = static_cast<int>(i % kRowsInStages);
+        mbar_arrive_expect_tx(bar0 + 8 * st, c.in_bytes);
+        bulk_load_g2s(in0 + st * kRowsCap, reinterpret_cast<const void *>(c.load), c.in_bytes, bar0 + 8 * st);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kRowsInStages; ++st) mbar_init(bar0 + 8 * st, 1);
+        fence_mbar_init();
+        for (int64_t i = 0; i < mine && i < kRowsInStages; ++i) issue(i);
+    }
+    __syncthreads();
+    int64_t issued = mine < kRowsInStages ? mine : kRowsInStages;
+    int64_t i = 0;
+    for (; i < mine; ++i) {
+        const int st = static_cast<int>(i % kRowsInStages);
+        const uint32_t parity = static_cast<uint32_t>((i / kRowsInStages) & 1);
+        const uint32_t ob = out0 + static_cast<uint32_t>(i % kRowsOut) * kRowsCap;
+        bool late = false;
+        if (!mbar_try_wait(bar0 + 8 * st, parity)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar0 + 8 * st, parity))
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    late = true;
+                    break;
+                }
+        }
+        int64_t k;
+        const RowsJob &j = job_of(i, k);
+        const RowsChunk c = rows_chunk(j, k);
+        if (!late) {
+            // Output unit u = (row rr, 16-byte unit c8) holds 8 fp16 whose
+            // source starts at byte shift + 2 * (rr * cols + 8 * c8) of the
+            // stage.  Each thread walks units tid, tid + T, ... carrying
+            // (rr, c8) forward instead of dividing per unit.
+            const uint32_t ib = in0 + st * kRowsCap;
+            const uint32_t per_row = static_cast<uint32_t>(j.pitch / 8);
+            const uint32_t cols = static_cast<uint32_t>(j.cols);
+            const uint32_t units = static_cast<uint32_t>(c.rows) * per_row;
+            const uint32_t step_r = kRowsThreads / per_row, step_c = kRowsThreads - step_r * per_row;
+            uint32_t rr = threadIdx.x / per_row, c8 = threadIdx.x - rr * per_row;
+            for (uint32_t u = threadIdx.x; u < units; u += kRowsThreads) {
+                const uint32_t b = c.shift + 2 * (rr * cols + 8 * c8);
+                const uint32_t sh = b & 15u, ba = b & ~15u, col = 8 * c8;
+                const uint4 lo = ld_shared_v4(ib + ba);
+                const uint4 hi = sh ? ld_shared_v4(ib + ba + 16) : make_uint4(0, 0, 0, 0);
+                uint32_t o[4];
+                realign16(lo, hi, sh, o);
+                if (col + 8 > cols) {
+                    const int valid = col < cols ? static_cast<int>(cols - col) : 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t keep =
+                            (2 * q < valid ? 0x0000FFFFu : 0u) | (2 * q + 1 < valid ? 0xFFFF0000u : 0u);
+                        o[q] &= keep;
+                    }
+                }
+                st_shared_v4(ob + 16 * u, o[0], o[1], o[2], o[3]);
+                c8 += step_c;
+                rr += step_r;
+                if (c8 >= per_row) {
+                    c8 -= per_row;
+                    ++rr;
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        if (__syncthreads_or(late)) break;
+        if (threadIdx.x == 0) {
+            bulk_store_s2g(c.dst, ob, c.out_bytes);
+            bulk_commit();
+            if (issued < mine) {
+                issue(issued);
+                ++issued;
+            }
+            bulk_wait_read<kRowsOut - 2>();  // frees the buffer of chunk i + 2
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (i < mine) {
+            atomicCAS(status, 0, static_cast<int>(GEMMPIPE_ERR_TIMEOUT));
+            for (int64_t q = i; q < issued; ++q) {
+                const int st = static_cast<int>(q % kRowsInStages);
+                const uint32_t parity = static_cast<uint32_t>((q / kRowsInStages) & 1);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar0 + 8 * st, parity))
+                    if (globaltimer_ns() - t0 > timeout_ns) break;
+            }
+        }
+        bulk_wait<0>();
+    }
+    __syncthreads();
 }
 
 __global__ void zero_fill_kernel(uint8_t *dst, int64_t bytes)
@@ -424,11 +588,54 @@ cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, u
                       ja, jb);
 }
 
+// Whole rows per bulk-copy chunk, 0 when a row does not fit a stage (the
+// fetched granules of R rows span at most 2*R*cols + 30 bytes and the
+// realigning reads look 16 bytes past the last output unit's source).
+int64_t rows_per_chunk(int64_t cols, int64_t pitch, const uint16_t *dst)
+{
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) != 0 || pitch % 8 != 0) return 0;
+    const int64_t w = 2 * (cols > pitch ? cols : pitch);
+    return (kRowsCap - 64) / w;
+}
+
 cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
                            const uint16_t *src1, int64_t rows1, int64_t cols1, uint16_t *dst1, int64_t pitch1,
                            int sms, cudaStream_t s)
 {
     // rows1 == 0: one job only.
+    const int64_t r0 = rows_per_chunk(cols0, pitch0, dst0);
+    const int64_t r1 = rows1 > 0 ? rows_per_chunk(cols1, pitch1, dst1) : 1;
+    if (r0 > 0 && r1 > 0 && rows0 > 0) {
+        static std::atomic<int> attr_done[128];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+        if (!attr_done[dev].load()) {
+            e = cudaFuncSetAttribute(pad_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem);
+            if (e != cudaSuccess) return e;
+            attr_done[dev].store(1);
+        }
+        int *st = nullptr;
+        if ((e = status_word(&st)) != cudaSuccess) return e;
+        const RowsJob a{src0, rows0, cols0, dst0, pitch0, r0};
+        const RowsJob b{src1, rows1, cols1, dst1, pitch1, r1};
+        const int64_t chunks = (rows0 + r0 - 1) / r0 + (rows1 > 0 ? (rows1 + r1 - 1) / r1 : 0);
+        const int grid = static_cast<int>(chunks < sms ? chunks : sms);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid > 0 ? grid : 1, 1, 1);
+        cfg.blockDim = dim3(kRowsThreads, 1, 1);
+        cfg.dynamicSmemBytes = kRowsSmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, pad_rows_kernel, a, b, st, static_cast<uint64_t>(2000000000ull));
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const PadJob j0{src0, rows0, cols0, dst0, pitch0};
     const PadJob j1{src1, rows1, cols1, dst1, pitch1};
     const int threads = 128;
