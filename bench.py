@@ -474,6 +474,8 @@ ABLATION = [
     ("int8: widening pass + pair, every tile whole", "s8", SQUARE, -1, 0, 0, -1, 0),
     ("int8: in-kernel widening, pair", "s8", SQUARE, 0, 256, 4, 1, -1),
     ("int8: in-kernel widening, single CTA", "s8", SQUARE, 0, 256, 2, 0, -1),
+    ("int8: the pages' design: mma.sync m16n8k32 + 4-stage cp.async ring", "s8", SQUARE, 2, 0, 0, -1, -1),
+    ("int8: the pages' design with their double buffer (S=2)", "s8", SQUARE, 2, 0, 2, -1, -1),
     ("ragged fp16: stream-K (default)", "f16", RAGGED, -1, 0, 0, -1, -1),
     ("ragged fp16: every tile whole", "f16", RAGGED, -1, 0, 0, -1, 0),
     ("skinny fp16: TMA producer (default)", "f16", SKINNY, -1, 0, 0, -1, -1),

@@ -204,7 +204,8 @@ GEMMPIPE_API int64_t gemmpipe_stage_smem_bytes(int BM, int BN, int BK, int elem_
 
 /* Kernel plan chosen for one call; filled by gemmpipe_plan(). */
 typedef struct {
-    int producer;        /* 0: TMA producer warp, 1: bounded-load (LDG) producer warps */
+    int producer;        /* 0: TMA producer warp, 1: bounded-load (LDG) producer warps,
+                            2: warp-level integer MMA with a cp.async ring (comparison path) */
     int BM, BN, BK;      /* output tile (BM = 256 for a CTA pair) and k-block */
     int stages;          /* depth S of the shared-memory ring */
     int k_chunk;         /* k values accumulated in one TMEM accumulator before a drain */
@@ -218,7 +219,8 @@ typedef struct {
     int64_t smem_bytes;  /* dynamic shared memory per CTA */
     int vector_store;    /* 1: 16-byte stores of C, 0: 4-byte stores */
     int operand_copy;    /* 0: none (INT8: widened in the kernel), 1: int8 widened to fp16 in the
-                            workspace, 2: misaligned fp16 padded in the workspace */
+                            workspace, 2: misaligned fp16 padded in the workspace,
+                            3: int8 B transposed in the workspace (producer 2) */
     int64_t workspace_bytes; /* library workspace the call needs (operand copies + split partial sums) */
 } gemmpipe_plan_t;
 
@@ -239,7 +241,11 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * stage/producer ablation).  producer: -1 automatic, 0 TMA (only honoured
  * where TMA can describe the operands; for gemm_s8s8s32 it selects the
  * in-kernel widening of int8 tiles), 1 bounded-load producer for
- * gemm_f16f32 and the workspace-widening path for gemm_s8s8s32.  bn: 0
+ * gemm_f16f32 and the workspace-widening path for gemm_s8s8s32, 2 (for
+ * gemm_s8s8s32 with A on a 16-byte boundary and K a multiple of 16) the
+ * pages' own design as a comparison path: warp-level integer MMA
+ * (mma.sync m16n8k32) fed by a 4-stage cp.async ring, on A and a transposed
+ * copy of B in the workspace (N x K bytes); exact like the other paths.  bn: 0
  * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
  * ring depths (when the chosen variant has no such depth the automatic one
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,

@@ -23,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgemmpipe.so")
 
-SOURCES = ["gemm_f16.cu", "gemm_s8.cu", "aux_kernels.cu", "gemmpipe_api.cpp", "gemm_noalloc.cu"]
+SOURCES = ["gemm_f16.cu", "gemm_s8.cu", "aux_kernels.cu", "gemmpipe_api.cpp", "gemm_noalloc.cu", "gemm_imma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
           "-I" + INCLUDE, "-I" + CSRC]

@@ -196,6 +196,19 @@ bool s8_convert_ok(const void *A, int64_t K, const void *B, int64_t N)
     return g_override.producer == 0;
 }
 
+// The legacy warp-MMA INT8 path (producer override 2): A read in place,
+// B transposed into the workspace.
+bool imma_wanted(const int8_t *A, int64_t K)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_override.producer != 2) return false;
+    }
+    return gp::imma_supported(A, K);
+}
+
+int64_t imma_workspace_bytes(int64_t N, int64_t K) { return N * gp::imma_bt_pitch(K); }
+
 // The plan of one GEMM.  fp16 operands (or INT8 calls' widened copies) when
 // convert is false; int8 operands read by TMA and widened in the kernel when
 // convert is true.
@@ -668,6 +681,31 @@ gemmpipe_status_t gemm_s8s8s32(int64_t M, int64_t N, int64_t K, const int8_t *A,
     if ((st = check_device_pointers(K, A, B, C, 1, 4)) != GEMMPIPE_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, M * N * 4, d, s);
+    if (imma_wanted(A, K)) {
+        // Comparison path: B transposed, then warp-level integer MMA.
+        const int64_t ldbt = gp::imma_bt_pitch(K);
+        void *ws = nullptr;
+        if ((st = workspace(dev, s, imma_workspace_bytes(N, K), &ws)) != GEMMPIPE_OK) return st;
+        int8_t *BT = static_cast<int8_t *>(ws);
+        {
+            TimedRegion tr(false, s);
+            const cudaError_t e = gp::launch_transpose_s8(B, K, N, BT, ldbt, s);
+            tr.end();
+            if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+            g_launches.fetch_add(1);
+        }
+        TimedRegion tr(true, s);
+        int stages = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            stages = g_override.stages;
+        }
+        const cudaError_t e = gp::launch_imma_s8(A, BT, ldbt, C, M, N, K, stages, s);
+        tr.end();
+        if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+        g_launches.fetch_add(1);
+        return GEMMPIPE_OK;
+    }
     if (s8_convert_ok(A, K, B, N)) {
         // int8 tiles straight from A and B, widened inside the kernel.
         Plan pl;
@@ -764,6 +802,31 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     std::memset(plan, 0, sizeof(*plan));
     if (M == 0 || N == 0 || K == 0) return GEMMPIPE_OK;
     Plan pl;
+    if (s8 && imma_wanted(static_cast<const int8_t *>(A), K)) {
+        gp::VariantInfo f;
+        int stages = 0;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            stages = g_override.stages;
+        }
+        gp::imma_plan_info(&f, stages);
+        plan->producer = f.producer;
+        plan->BM = f.BM;
+        plan->BN = f.BN;
+        plan->BK = f.BK;
+        plan->stages = f.stages;
+        plan->k_chunk = static_cast<int>(K);
+        plan->threads = f.threads;
+        plan->tiles = ((M + f.BM - 1) / f.BM) * ((N + f.BN - 1) / f.BN);
+        plan->grid = static_cast<int>(plan->tiles);
+        plan->units = plan->tiles;
+        plan->k_blocks = (K + f.BK - 1) / f.BK;
+        plan->smem_bytes = f.smem_bytes;
+        plan->vector_store = 0;
+        plan->operand_copy = 3;
+        plan->workspace_bytes = imma_workspace_bytes(N, K);
+        return GEMMPIPE_OK;
+    }
     if (s8 && s8_convert_ok(A, K, B, N)) {
         st = make_plan(true, M, N, K, A, K, B, N, C, N, d, &pl, true);
     } else if (s8) {
@@ -804,7 +867,7 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
 
 gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair, int split)
 {
-    if (producer < -1 || producer > 1) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (producer < -1 || producer > 2) return GEMMPIPE_ERR_INVALID_VALUE;
     if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
     if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;

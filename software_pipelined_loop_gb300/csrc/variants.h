@@ -46,6 +46,15 @@ cudaError_t launch_zero_fill(void *dst, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t launch_copy(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s);
 cudaError_t status_word(int **ptr);  // device address of the current device's status word
 
+// The legacy warp-MMA INT8 path (gemm_imma.cu): mma.sync m16n8k32 with a
+// cp.async ring, on A and a transposed copy of B (comparison path).
+bool imma_supported(const int8_t *A, int64_t K);
+int64_t imma_bt_pitch(int64_t K);
+cudaError_t launch_transpose_s8(const int8_t *B, int64_t K, int64_t N, int8_t *BT, int64_t ldbt, cudaStream_t s);
+cudaError_t launch_imma_s8(const int8_t *A, const int8_t *BT, int64_t ldbt, int32_t *C, int64_t M, int64_t N,
+                           int64_t K, int stages, cudaStream_t s);
+void imma_plan_info(VariantInfo *f, int stages);  // stages: 2, else the default 4
+
 // The INT8 flow with fixed, caller-provided scratch (gemmpipe_api.cpp), for
 // the no-allocation entry point.
 gemmpipe_status_t s8_check_fixed_scratch(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B,

@@ -591,3 +591,43 @@ def test_ring_depths_of_cta_pair(dev, stages):
     finally:
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert_f16_close(got, oracle.gemm_f16f32(A, B), f"S={stages}")
+
+
+# -------------------------------------- warp-level integer MMA (comparison)
+
+@pytest.mark.parametrize("stages", [4, 2], ids=["S4", "S2"])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 270, 1040), (1000, 777, 4096), (17, 33, 16),
+                                   (513, 129, 208), (2048, 2048, 2048)])
+def test_imma_comparison_path_is_bit_exact(dev, M, N, K, stages):
+    # The pages' design (mma.sync m16n8k32 s8 with a cp.async ring; S = 2 is
+    # their double buffer) on A and a transposed copy of B: bit-exact like
+    # the tcgen05 paths.
+    A, B = inputs.make_operands("s8", M, N, K, seed=1100 + M + N + K)
+    gemmpipe.gemmpipe_set_plan_override(2, 0, stages if stages == 2 else 0)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0, M, N, K)
+        assert plan["producer"] == 2 and plan["operand_copy"] == 3 and plan["stages"] == stages
+        assert plan["workspace_bytes"] == N * (-(-K // 16) * 16)
+        got = run_s8(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B))
+
+
+def test_imma_comparison_path_extremes_and_fallback(dev):
+    M, N, K = 200, 136, 4096
+    A = np.full((M, K), -128, dtype=np.int8)
+    B = np.full((K, N), -128, dtype=np.int8)
+    gemmpipe.gemmpipe_set_plan_override(2, 0, 0)
+    try:
+        got = run_s8(A, B, dev)
+        # K not a multiple of 16: the comparison path does not apply and the
+        # call takes the default widening path.
+        plan = gemmpipe.gemmpipe_plan(0, 64, 64, 100)
+        assert plan["producer"] == 0 and plan["operand_copy"] == 1
+        A2, B2 = inputs.make_operands("s8", 64, 64, 100, seed=5)
+        got2 = run_s8(A2, B2, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    assert (got == 16384 * K).all()
+    np.testing.assert_array_equal(got2, oracle.gemm_s8s8s32(A2, B2))
