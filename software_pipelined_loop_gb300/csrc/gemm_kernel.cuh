@@ -802,10 +802,27 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
 // (16-byte chunks XOR-swizzled by row, conflict-free both ways) so that each
 // global store instruction writes whole 128-byte row pieces.
 template <bool ADD = false>
-__device__ __forceinline__ void store_block(const GemmParams &p, uint32_t stg, const uint32_t *r,
-                                            int64_t row0, int64_t col0, int lane)
+__device__ __forceinline__ void store_block(const GemmParams &p, const CUtensorMap *tC, uint32_t stg,
+                                            const uint32_t *r, int64_t row0, int64_t col0, int lane)
 {
     if (row0 >= p.M || col0 >= p.N) return;  // warp-uniform
+    if (!ADD && p.tma_store) {
+        // The staging tile is in the 128-byte swizzle the C tensor map
+        // declares; one TMA store writes the block (clipped at M and N).
+        if (lane == 0) bulk_wait_read<0>();  // the previous block's store has read the tile
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                         r[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tC, stg, static_cast<int32_t>(col0), static_cast<int32_t>(row0));
+            bulk_commit();
+        }
+        return;
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c)
         st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
@@ -928,8 +945,8 @@ __device__ __forceinline__ int64_t first_part_unit(const GemmParams &p, int64_t 
 }
 
 template <class Cfg>
-__device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl,
-                         const Waiter &w, int warp, int lane, uint32_t rank)
+__device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sbase, uint32_t tmem_base,
+                         Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, int warp, int lane, uint32_t rank)
 {
     const int e = warp - Cfg::EPI_WARP0;  // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
@@ -1001,9 +1018,9 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
                     if (kc == wk.kb0)
-                        store_block<false>(p, stg, r, row0, colb + jb * 32, lane);
+                        store_block<false>(p, tC, stg, r, row0, colb + jb * 32, lane);
                     else
-                        store_block<true>(p, stg, r, row0, colb + jb * 32, lane);
+                        store_block<true>(p, tC, stg, r, row0, colb + jb * 32, lane);
                 }
             } else if constexpr (ISUM) {
                 // Chunk partials are integers below 2^24 in magnitude: exact
@@ -1033,7 +1050,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
                     } else {
                         for (int64_t v = me - 1; v >= v_lo; --v)
                             add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), r, lane);
-                        store_block(p, stg, r, row0, colb + jb * 32, lane);
+                        store_block(p, tC, stg, r, row0, colb + jb * 32, lane);
                     }
                 }
             }
@@ -1055,7 +1072,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
                 if (wk.kind == 1)
                     write_part(part_block<Cfg>(p, my_slot, e, jb), &val[jb * 32], lane);
                 else
-                    store_block(p, stg, &val[jb * 32], row0, colb + jb * 32, lane);
+                    store_block(p, tC, stg, &val[jb * 32], row0, colb + jb * 32, lane);
             }
         }
         if (wk.kind == 1) {
@@ -1072,7 +1089,7 @@ __device__ void epilogue(const GemmParams &p, uint32_t sbase, uint32_t tmem_base
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_pipelined_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const GemmParams p)
+                          const __grid_constant__ CUtensorMap tmC, const GemmParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1113,6 +1130,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (threadIdx.x == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (p.tma_store) tma_prefetch_desc(&tmC);
         }
     }
     tc_fence_before_sync();
@@ -1147,7 +1165,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         } else {
             setmaxnreg_inc<Cfg::EPI_REGS>();
-            epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane, rank);
+            epilogue<Cfg>(p, &tmC, sbase, tmem_base, ctl, w, warp, lane, rank);
+            if (lane == 0) bulk_wait<0>();  // every C store issued by this warp has completed
+            __syncwarp();
         }
     } else if (warp < Cfg::PRODUCER_WARPS) {
         if constexpr (Cfg::LDG) {
@@ -1165,7 +1185,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         __syncwarp();
     } else {
-        epilogue<Cfg>(p, sbase, tmem_base, ctl, w, warp, lane, rank);
+        epilogue<Cfg>(p, &tmC, sbase, tmem_base, ctl, w, warp, lane, rank);
+        if (lane == 0) bulk_wait<0>();  // every C store issued by this warp has completed
+        __syncwarp();
     }
 
     tc_fence_before_sync();

@@ -31,6 +31,7 @@ struct GemmParams {
     int64_t num_kb;        // ceil(K / BK)
     int64_t kb_per_chunk;  // k-blocks per TMEM accumulation unit
     int vec_store;         // C base and pitch allow 16-byte stores
+    int tma_store;         // C blocks leave through TMA bulk-tensor stores (the C tensor map is valid)
     int64_t stall_kb;      // test hook: CTA 0 leaves this k-block unfilled (-1: none)
     uint64_t timeout_ns;   // bound of every pipeline wait
     int *status;           // device status word

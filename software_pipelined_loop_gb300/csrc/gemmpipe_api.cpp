@@ -331,6 +331,21 @@ bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int
     return encode_2d_any(m, base, rows, cols, ld, 64, box_rows, false);
 }
 
+// C (rows x cols of 4-byte elements, pitch ld) for the epilogue's TMA
+// stores: 32 x 32 boxes in the 128-byte swizzle of its staging tiles.
+bool encode_c(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld, bool int_out)
+{
+    EncodeFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 4)};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(m, int_out ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ timing
 
 struct Timing {
@@ -472,6 +487,8 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
         // same boxes for its half.
         if (!encode_2d(&ta, A, M, K, lda, kBM) || !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
     }
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
     GemmParams p;
     p.M = M;
     p.N = N;
@@ -483,6 +500,7 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
     p.C = C;
     p.ldc = ldc;
     set_schedule(pl, dev, s, p);
+    p.tma_store = pl.vec_store && encode_c(&tc, C, M, N, ldc, pl.v->info.int_out != 0) ? 1 : 0;
     p.stall_kb = -1;
     p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
     {
@@ -498,7 +516,7 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
         return GEMMPIPE_ERR_LAUNCH;
     }
     TimedRegion tr(true, s);
-    const cudaError_t e = pl.v->launch(ta, tb, p, pl.grid, s);
+    const cudaError_t e = pl.v->launch(ta, tb, tc, p, pl.grid, s);
     tr.end();
     if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
@@ -608,13 +626,16 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
     p.num_kb = pl.num_kb;
     p.kb_per_chunk = pl.kb_per_chunk;
     p.vec_store = pl.vec_store;
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    p.tma_store = pl.vec_store && encode_c(&tc, C, M, N, N, true) ? 1 : 0;
     p.stall_kb = -1;
     p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
     if (gp::status_word(&p.status) != cudaSuccess) {
         cudaGetLastError();
         return GEMMPIPE_ERR_LAUNCH;
     }
-    if (pl.v->launch(ta, tb, p, pl.grid, s) != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+    if (pl.v->launch(ta, tb, tc, p, pl.grid, s) != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
     return GEMMPIPE_OK;
 }

@@ -9,7 +9,8 @@
 namespace gp {
 
 template <class Cfg>
-cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid, cudaStream_t s)
+cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const GemmParams &p, int grid,
+                       cudaStream_t s)
 {
     static std::atomic<int> attr_done[128];
     int dev = 0;
@@ -51,7 +52,7 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const GemmPar
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    e = cudaLaunchKernelEx(&cfg, gemm_pipelined_kernel<Cfg>, a, b, p);
+    e = cudaLaunchKernelEx(&cfg, gemm_pipelined_kernel<Cfg>, a, b, c, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -21,8 +21,8 @@ struct VariantInfo {
     int split_ok;  // 1: the epilogue can take split (stream-K) tiles
 };
 
-using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const GemmParams &, int grid,
-                                 cudaStream_t);
+using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmParams &,
+                                 int grid, cudaStream_t);
 using ClustersFn = int (*)();  // co-resident CTA pairs on the current device (pair variants)
 
 struct Variant {
