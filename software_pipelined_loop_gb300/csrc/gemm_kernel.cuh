@@ -265,8 +265,15 @@ struct WorkIter {
         } else {
             return false;
         }
-        w.m0 = (tile % p.m_tiles) * Cfg::TILE_M;
-        w.n0 = (tile / p.m_tiles) * Cfg::BN;
+        // Grouped order: tile -> (group, index in group); a group holds
+        // gm tile rows (the last one may hold fewer) times all columns.
+        const int64_t n_tiles = p.tiles / p.m_tiles;
+        const int64_t per_group = p.group_m * n_tiles;
+        const int64_t g = tile / per_group, in = tile - g * per_group;
+        const int64_t first = g * p.group_m;
+        const int64_t gm = p.m_tiles - first < p.group_m ? p.m_tiles - first : p.group_m;
+        w.m0 = (first + in % gm) * Cfg::TILE_M;
+        w.n0 = (in / gm) * Cfg::BN;
         return true;
     }
 };

@@ -14,7 +14,11 @@ struct GemmParams {
     int64_t ldb;
     void *C;  // float or int32, M x N, row pitch ldc elements
     int64_t ldc;
-    int64_t m_tiles, tiles;  // tile grid (m fastest); a tile is 128 or 256 (CTA pair) rows x BN
+    int64_t m_tiles, tiles;  // tile grid; a tile is 128 or 256 (CTA pair) rows x BN
+    // Tile order: groups of group_m tile rows, m fastest inside a group and
+    // the group's columns in turn, so the tiles in flight at once share a
+    // few rows of A and columns of B (an L2-sized working set).
+    int64_t group_m;
     // Persistent schedule over `units` (CTAs, or CTA pairs): tiles
     // [0, dp_tiles) go whole and round-robin; the k-blocks of the remaining
     // tiles (sk_work = their count times num_kb, tile-major) are split into

@@ -126,7 +126,7 @@ StallHook g_stall;
 struct Plan {
     const Variant *v = nullptr;
     int grid = 0;
-    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0;
+    int64_t tiles = 0, m_tiles = 0, num_kb = 0, kb_per_chunk = 0, group_m = 1;
     int64_t units = 0, dp_tiles = 0, sk_tiles = 0;
     int64_t slots = 0;  // co-resident units (CTAs or CTA pairs)
     int vec_store = 0;
@@ -277,6 +277,11 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
         pl->dp_tiles = T - pl->sk_tiles;
     }
     pl->grid = static_cast<int>(v->info.pair ? 2 * pl->units : pl->units);
+    // Tile rows per group ~ sqrt(units): the tiles of a wave then cover
+    // about sqrt(units) panels of A and as many of B, the fewest bytes.
+    int64_t gm = 1;
+    while ((gm + 1) * (gm + 1) <= pl->units) ++gm;
+    pl->group_m = gm < pl->m_tiles ? gm : pl->m_tiles;
     pl->vec_store = aligned16(C) && (ldc * 4) % 16 == 0;
     return GEMMPIPE_OK;
 }
@@ -462,6 +467,7 @@ void set_schedule(Plan &pl, int dev, cudaStream_t s, GemmParams &p)
     }
     p.m_tiles = pl.m_tiles;
     p.tiles = pl.tiles;
+    p.group_m = pl.group_m;
     p.units = pl.units;
     p.dp_tiles = pl.dp_tiles;
     p.sk_work = pl.sk_tiles * pl.num_kb;
@@ -617,6 +623,7 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
     p.ldc = N;
     p.m_tiles = pl.m_tiles;
     p.tiles = pl.tiles;
+    p.group_m = pl.group_m;
     p.units = pl.units;
     p.dp_tiles = pl.dp_tiles;
     p.sk_work = 0;

@@ -128,3 +128,28 @@ def test_balance_when_tiles_overflow_the_grid():
         units, dp, sk = plan(tiles, slots, num_kb)
         work = [sum(kb1 - kb0 for (_, kb0, kb1, _) in items(u, units, dp, sk, num_kb)) for u in range(units)]
         assert max(work) - min(work) <= 1
+
+
+def tile_coords(tile: int, m_tiles: int, n_tiles: int, group_m: int) -> tuple[int, int]:
+    """The kernel's grouped tile order: group_m tile rows at a time, m
+    fastest inside a group."""
+    per_group = group_m * n_tiles
+    g, i = divmod(tile, per_group)
+    first = g * group_m
+    gm = min(group_m, m_tiles - first)
+    return first + i % gm, i // gm
+
+
+@pytest.mark.parametrize("m_tiles,n_tiles", [(1, 1), (16, 16), (16, 12), (32, 32), (5, 7), (64, 1), (1, 64)])
+@pytest.mark.parametrize("units", [1, 8, 76, 152])
+def test_grouped_tile_order_is_a_bijection(m_tiles, n_tiles, units):
+    gm = 1
+    while (gm + 1) ** 2 <= units:
+        gm += 1
+    gm = min(gm, m_tiles)
+    seen = {tile_coords(t, m_tiles, n_tiles, gm) for t in range(m_tiles * n_tiles)}
+    assert seen == {(m, n) for m in range(m_tiles) for n in range(n_tiles)}
+    if m_tiles == n_tiles == 32 and units == 76:
+        # A wave of 76 tiles touches 8 rows of A panels and 10 columns of B.
+        wave = {tile_coords(t, m_tiles, n_tiles, gm) for t in range(76)}
+        assert len({m for m, _ in wave}) == 8 and len({n for _, n in wave}) == 10
