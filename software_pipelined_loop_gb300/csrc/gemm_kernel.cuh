@@ -675,6 +675,15 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
             }
         }
     }
+    if (ok) {
+        // The MMA commits of the last k-blocks arrive on this CTA's empty
+        // barriers (the peer's from the leader's tensor cores): wait for
+        // each stage's last phase so none is still in flight at exit.
+        for (int s = 0; s < Cfg::STAGES && ok; ++s) {
+            const uint32_t ph = s < stage ? phase ^ 1u : phase;  // phase of the stage's next use
+            ok = w.wait(smem_u32(&ctl->empty[s]), ph ^ 1u);
+        }
+    }
     if (!ok) {
         if (rank == 0) {
             // The leader's full barriers count both CTAs' copies.
@@ -739,6 +748,14 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+    }
+    if (ok) {
+        // Both accumulators' last releases -- including the peer's
+        // epilogue arrivals on these barriers -- have landed before the
+        // pair's final (relaxed) cluster barrier.  The parities are the
+        // ones the next use of each buffer would wait for.
+        ok = w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u) &&
+             w.wait(smem_u32(&ctl->tempty[acc ^ 1u]), acc == 0 ? acc_phase ^ 1u : acc_phase);
     }
     if (!ok && issued) {
         umma_commit_pair(smem_u32(&ctl->drain), 1);
@@ -1199,7 +1216,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (Cfg::PAIR) cluster_sync();  // no peer still signals or reads this CTA
+    if constexpr (Cfg::PAIR) {
+        // No peer still signals or reads this CTA after the barrier.  On
+        // the normal path every cross-CTA arrival has already been observed
+        // (the leader waited for the accumulators' last releases, the
+        // producers for their stages' last MMA commits), so the barrier
+        // needs no release ordering.  A CTA that aborted keeps it (a wait
+        // that ran out in one CTA leaves its peer waiting on arrivals that
+        // never come, so that one aborts too).
+        const bool aborted = *reinterpret_cast<volatile int *>(&ctl->abort) != 0;
+        if (!Cfg::REG_SPLIT || __syncthreads_or(aborted))
+            cluster_sync();
+        else
+            cluster_sync_relaxed();
+    }
     if (warp == Cfg::MMA_WARP) {
         tc_fence_after_sync();
         if constexpr (Cfg::PAIR)

@@ -314,6 +314,22 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// 32-bit load from a cluster shared-memory address (mapa_shared).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Cluster barrier without release ordering: for the end of a pair's work,
+// once every cross-CTA arrival has been observed through its mbarrier (a
+// release arrive there waits several microseconds for the memory system).
+__device__ __forceinline__ void cluster_sync_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in
 // the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
