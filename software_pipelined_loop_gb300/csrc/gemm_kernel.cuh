@@ -7,22 +7,30 @@
 // Here the same schedule is spread over warps with separate jobs and the
 // double buffer becomes an S-stage ring guarded by mbarriers:
 //
-//   producer  (1 warp issuing TMA tile loads, or 8 warps doing bounds-checked
-//             loads into registers and shared-memory stores -- the page's
-//             LDG-register variant, used when TMA cannot describe the input)
-//             waits empty[s], fills stage s with the A tile (BM x BK) and the
-//             B tile (BK x BN) of k-block kb, and signals full[s];
-//   issuer    (one thread) waits full[s], issues BK/16 tcgen05.mma
-//             (M = 128, N = BN, K = 16) into a TMEM accumulator, then
-//             tcgen05.commit -> empty[s] returns the stage to the producer
-//             as soon as the tensor cores have read it;
-//   epilogue  (8 warps) waits tfull[b], reads the accumulator with
-//             tcgen05.ld, and stores C through a per-warp staging tile so
-//             that the global stores are row-contiguous.
+//   producer  (1 thread issuing TMA tile loads, or 8 warps doing
+//             bounds-checked loads into registers and shared-memory stores --
+//             the page's LDG-register variant, used when TMA cannot describe
+//             the input) waits empty[s], fills stage s with the A tile
+//             (BM x BK) and the B tile (BK x BN) of k-block kb, and signals
+//             full[s];
+//   issuer    (one thread) waits full[s], issues BK/16 tcgen05.mma (K = 16;
+//             M = 256 over a CTA pair with cta_group::2, else 128) into a
+//             TMEM accumulator, then tcgen05.commit -> empty[s] returns the
+//             stage to the producer as soon as the tensor cores have read it;
+//   epilogue  (8 warps) waits tfull[b], copies the accumulator to registers
+//             with tcgen05.ld, frees it, and stores C through a per-warp
+//             staging tile (one TMA store per 32 x 32 block, or
+//             row-contiguous masked stores).
 //
 // The page's prologue is the producer running up to S stages ahead; its
 // "compute the last tile" epilogue is the issuer's final commit on tfull.
 // Two TMEM accumulators let tile t+1's MMAs run while tile t is stored.
+//
+// The CTAs are persistent (one per SM, or one pair per two SMs) and walk a
+// static schedule (WorkIter): whole tiles round-robin, then equal ranges of
+// the split tiles' k-blocks (stream-K), whose partial sums meet in a
+// workspace.  TMA variants run 12 warps: warps 0-3 (producer, issuer, two
+// idle) give registers to the two epilogue warpgroups with setmaxnreg.
 //
 // For the INT8 path (operands widened to fp16, see the C header) an
 // accumulator covers at most `kb_per_chunk` k-blocks; the epilogue turns
