@@ -48,8 +48,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu"]
 TRAFFIC = {
     # (int8 operands, cta pair, BN): (bytes per launch, sources hash, profile)
-    ("s8", 1, 256): (132_613_120, "430b322427983b15", "profiles/gemm_pair_int8_4096.md"),
-    ("f16", 1, 256): (133_891_072, "430b322427983b15", "profiles/gemm_pair_f16_4096.md"),
+    ("s8", 1, 256): (138_815_232, "61e6ac4fb09ee2ce", "profiles/gemm_pair_int8_4096.md"),
+    ("f16", 1, 256): (140_950_784, "61e6ac4fb09ee2ce", "profiles/gemm_pair_f16_4096.md"),
 }
 
 
