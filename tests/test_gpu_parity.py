@@ -631,3 +631,52 @@ def test_imma_comparison_path_extremes_and_fallback(dev):
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert (got == 16384 * K).all()
     np.testing.assert_array_equal(got2, oracle.gemm_s8s8s32(A2, B2))
+
+
+# ------------------------------------------- int32 wrap and 64-bit indexing
+
+@pytest.mark.parametrize("path", ["tcgen05", "imma"])
+def test_s8_sums_wrap_modulo_2_32(dev, path):
+    # K = 2^17 + 64 with extreme operands: exact sums up to 16384 * K exceed
+    # int32 and wrap modulo 2^32, as integer hardware does.  One 64 x 64
+    # tile over 2049 k-blocks: the tcgen05 path splits it over the whole
+    # grid (a finisher adding up to ~150 partial sums).
+    M, N, K = 64, 64, (1 << 17) + 64
+    rng = np.random.default_rng(11)
+    A = np.where(rng.random((M, K)) < 0.9, -128, 127).astype(np.int8)
+    B = np.where(rng.random((K, N)) < 0.9, -128, 127).astype(np.int8)
+    A[0, :] = -128
+    B[:, 0] = -128
+    want = oracle.gemm_s8s8s32(A, B, allow_overflow=True)
+    assert want[0, 0] == np.int32(np.int64(16384 * K) - (1 << 32))
+    gemmpipe.gemmpipe_set_plan_override(2 if path == "imma" else -1, 0, 0)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0, M, N, K)
+        if path == "tcgen05":
+            assert plan["split_tiles"] == 1 and plan["units"] > 100
+        got = run_s8(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+def test_c_beyond_2_31_elements(dev, dtype):
+    # C of 600000 x 4096 = 2.46e9 elements (9.8 GB): row offsets past 2^31
+    # elements on every path (TMA store coordinates, partial sums, widening).
+    import torch
+    M, N, K = 600000, 4096, 64
+    A, B = inputs.make_operands(dtype, M, N, K, seed=77)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.empty((M, N), dtype=torch.int32 if dtype == "s8" else torch.float32, device=dev)
+    C[-1].fill_(-7)
+    (gemmpipe.gemm_s8s8s32 if dtype == "s8" else gemmpipe.gemm_f16f32)(M, N, K, Ad, Bd, C)
+    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    rows = sample_rows(M)
+    idx = torch.from_numpy(rows).to(dev)
+    got = C.index_select(0, idx).cpu().numpy()
+    del C
+    if dtype == "s8":
+        np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B, rows=rows))
+    else:
+        assert_f16_close(got, oracle.gemm_f16f32(A, B, rows=rows))
