@@ -287,13 +287,17 @@ def measure_gemm(wl, steps: int, warmup: int, dev, flush, peaks, peak_src):
         "ops_per_s": flops / ms / 1e9, "bytes_per_s": alg_bytes / ms / 1e6, "kernel_ms": kernel_ms,
         "aux_ms": aux_ms / max(1, aux_n) if aux_n else 0.0, "launches": launches, "flops": flops,
         "alg_bytes": alg_bytes, "roofline": roof, "plan": plan, "l2": "flushed" if needs_flush else "inputs > L2",
-        "window": (t0, t1), "A": A, "B": B,
+        "window": (t0, t1), "A": A, "B": B, "C": C,
     }
 
 
 def measure_e2e(res: dict, steps: int, dev) -> dict:
-    """Same GEMM through the C ABI with host buffers: pinned H2D of A and B,
-    the call, D2H of C, all inside the event-timed region."""
+    """Same GEMM through the C ABI's host-buffer call (gemm_s8s8s32_host /
+    gemm_f16f32_host): A and B from page-locked host memory to the GPU, the
+    GEMM, C back to page-locked host memory, all inside the event-timed
+    region (the library overlaps the three by row panels).  Its C is
+    compared with the device-resident call's C (exact for INT8; FP16 plans
+    differ per panel, so within the FP16 tolerance)."""
     import torch
 
     from software_pipelined_loop_gb300 import gemmpipe
@@ -302,26 +306,48 @@ def measure_e2e(res: dict, steps: int, dev) -> dict:
     Bh = torch.from_numpy(B).pin_memory()
     out_dtype = torch.int32 if res["dtype"] == "s8" else torch.float32
     Ch = torch.empty((M, N), dtype=out_dtype).pin_memory()
-    Ad = torch.empty_like(Ah, device=dev)
-    Bd = torch.empty_like(Bh, device=dev)
-    Cd = torch.empty((M, N), dtype=out_dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
-    fn = gemmpipe.gemm_s8s8s32 if res["dtype"] == "s8" else gemmpipe.gemm_f16f32
-
-    def call():
-        Ad.copy_(Ah, non_blocking=True)
-        Bd.copy_(Bh, non_blocking=True)
-        fn(M, N, K, Ad, Bd, Cd, stream)
-        Ch.copy_(Cd, non_blocking=True)
-
+    fn = gemmpipe.gemm_s8s8s32_host if res["dtype"] == "s8" else gemmpipe.gemm_f16f32_host
+    call = lambda: fn(M, N, K, Ah, Bh, Ch, stream)
     for _ in range(3):
         call()
     torch.cuda.synchronize()
     times = time_steps(call, steps, None, stream)
+    st = gemmpipe.gemmpipe_get_device_status(stream)
+    if st != gemmpipe.OK:
+        raise RuntimeError(f"e2e: device status {gemmpipe.STATUS.get(st, st)}")
     ms = statistics.mean(times)
+    ref = res["C"].cpu()
+    if res["dtype"] == "s8":
+        same = bool(torch.equal(Ch, ref))
+    else:
+        same = bool((Ch.double() - ref.double()).abs().max().item() <= 1e-2)
+    if not same:
+        raise RuntimeError("e2e: the host-buffer call's C differs from the device-resident call's C")
     return {"value": res["flops"] / ms / 1e9, "unit": "TOPS" if res["dtype"] == "s8" else "TFLOPS",
             "ms_per_step": ms, "h2d_bytes_per_step": A.nbytes + B.nbytes,
-            "d2h_bytes_per_step": Ch.numel() * Ch.element_size()}
+            "d2h_bytes_per_step": Ch.numel() * Ch.element_size(),
+            "call": fn.__name__, "panel_rows": gemmpipe.gemmpipe_host_panel_rows(M)}
+
+
+def measure_copy_ref(dev, peaks: dict, reps: int = 10) -> dict:
+    """The in-run bandwidth reference: the library's plain copy kernel moving
+    512 MiB device to device (bytes read + bytes written per second)."""
+    import torch
+
+    from software_pipelined_loop_gb300 import gemmpipe
+    n = 512 << 20
+    src = torch.ones(n, dtype=torch.uint8, device=dev)
+    dst = torch.empty(n, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: gemmpipe.gemmpipe_copy(dst, src, n, stream)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ms = statistics.median(time_steps(call, reps, None, stream))
+    gbs = 2 * n / ms / 1e6
+    return {"kernel": "copy_kernel (16-byte loads and stores, grid-stride)", "bytes_moved": 2 * n,
+            "gbs": gbs, "of_measured_hbm_peak": gbs / peaks["hbm_gbs"]}
 
 
 def slowest_rank_ms(ms: float, dist=None, device=None) -> float:
@@ -391,6 +417,7 @@ def run_gpu(args) -> int:
                 r = measure_gemm(wl, max(10, args.steps // 4), args.warmup, dev, flush, peaks, peak_src)
                 secondary[r["name"]] = r
         e2e = measure_e2e(head, max(5, args.steps // 4), dev)
+        copy_ref = measure_copy_ref(dev, peaks)
     finally:
         clock.stop()
 
@@ -437,6 +464,7 @@ def run_gpu(args) -> int:
         "roofline": head["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "copy_ref": copy_ref,
         "gpu_launches": head["launches"],
         "clocks": clocks,
         "kernel_ms": head["kernel_ms"], "aux_ms": head["aux_ms"],

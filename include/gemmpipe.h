@@ -174,6 +174,55 @@ GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32_noalloc(int64_t M, int64_t N, int64_
                                                     gemmpipe_stream_t stream);
 
 /*
+ * The two GEMMs above with A, B and C in host memory: the call copies the
+ * operands to the GPU, computes C and copies it back, overlapping the three.
+ * The pages' method (loads of the next tile overlap the math on this one)
+ * applied one level up, between the host link and the GPU.
+ *
+ * Arguments, layout and result: as gemm_s8s8s32 / gemm_f16f32, except that
+ * A, B and C are host pointers (any pointer cudaMemcpy accepts: pageable or
+ * page-locked host memory, also managed or device memory).
+ *
+ * How: B is copied first, then A in row panels of gemmpipe_host_panel_rows(M)
+ * rows, on a copy stream of the library's; panel p's GEMM runs on `stream`
+ * as soon as its rows (and B) have arrived; its rows of C are copied back on
+ * a second library stream while later panels compute.  The INT8 call
+ * widens B once and each panel's rows of A as they arrive.
+ *
+ * Ordering and completion: the copies start after all work enqueued on
+ * `stream` before the call, and work enqueued on `stream` after the call
+ * starts after C has been written.  With page-locked A, B and C (e.g.
+ * cudaHostAlloc or cudaHostRegister) the call is asynchronous: synchronize
+ * `stream` before reading C.  With pageable memory the CUDA runtime makes
+ * the copies synchronous, so the call returns when C has been written (the
+ * copies back still overlap the later panels' GEMMs).  The caller keeps A,
+ * B and C allocated and A, B unchanged until then.  Calls on one stream
+ * from several host threads must be ordered by the caller.
+ *
+ * Memory: device buffers for A, B and C (M*K + K*N + M*N*4 bytes for INT8,
+ * 2*M*K + 2*K*N + 4*M*N for FP16) in a per-(device, stream) workspace, plus
+ * what the device-pointer call allocates; two library streams and a few
+ * events per (device, stream).  gemmpipe_release_workspaces frees them.
+ *
+ * Errors: as the device-pointer calls (GEMMPIPE_ERR_OUT_OF_MEMORY when the
+ * buffers do not fit); a failure after some copies were enqueued still
+ * leaves `stream` ordered after them.
+ */
+GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32_host(int64_t M, int64_t N, int64_t K,
+                                                 const int8_t *A, const int8_t *B, int32_t *C,
+                                                 gemmpipe_stream_t stream);
+GEMMPIPE_API gemmpipe_status_t gemm_f16f32_host(int64_t M, int64_t N, int64_t K,
+                                                const gemmpipe_half_t *A, const gemmpipe_half_t *B,
+                                                float *C, gemmpipe_stream_t stream);
+
+/*
+ * Rows per panel of the host-buffer calls: about an eighth of M rounded up
+ * to a multiple of 256, at least 512 (so M <= 512 is one panel).  Needs no
+ * GPU.
+ */
+GEMMPIPE_API int64_t gemmpipe_host_panel_rows(int64_t M);
+
+/*
  * Synchronizes `stream`, then reads and clears the current device's error
  * word.  Returns GEMMPIPE_ERR_TIMEOUT if a kernel of this library gave up on
  * a pipeline wait (every wait is bounded; the kernel then stops issuing
@@ -257,7 +306,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair,
                                                           int split);
 
-/* Frees every INT8 workspace (synchronizes the device first). */
+/* Frees every workspace of the library (operand copies, stream-K partial
+ * sums, host-call buffers) and the host calls' streams and events.  Call it
+ * with no work of the library in flight. */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_release_workspaces(void);
 
 /*

@@ -404,7 +404,7 @@ struct Workspace {
     int64_t bytes = 0;
 };
 // Kinds of workspace per (device, stream).
-enum WsKind { kWsOperands = 0, kWsSplit = 1 };
+enum WsKind { kWsOperands = 0, kWsSplit = 1, kWsHost = 2 };
 std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_ws;
 
 // The (device, stream) workspace of one kind, at least `bytes` long.  A new
@@ -649,7 +649,208 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
 
 }  // namespace gp
 
+namespace {
+
+// ------------------------------------------------------- host-buffer calls
+
+// Side streams and events of the host-buffer entry points, per (device,
+// caller stream): copies to the device run on `in`, copies back on `out`,
+// kernels on the caller's stream; events order the three.
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    std::vector<cudaEvent_t> ev;
+};
+std::map<std::pair<int, cudaStream_t>, HostPipe> g_host;
+
+gemmpipe_status_t host_pipe(int dev, cudaStream_t s, size_t events, HostPipe *out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    HostPipe &h = g_host[std::make_pair(dev, s)];
+    if (!h.in && cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        h.in = nullptr;
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    if (!h.out && cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        h.out = nullptr;
+        return GEMMPIPE_ERR_LAUNCH;
+    }
+    while (h.ev.size() < events) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMMPIPE_ERR_LAUNCH;
+        }
+        h.ev.push_back(e);
+    }
+    *out = h;
+    return GEMMPIPE_OK;
+}
+
+int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
+
+// One host-buffer call: B and the row panels of A go to device buffers on
+// the `in` stream, panel p's GEMM runs on the caller's stream once its rows
+// have arrived, and its rows of C go back on the `out` stream while later
+// panels compute.  `panel` enqueues the kernels of rows [r0, r0 + rows).
+// Everything is enqueued before the first copy back, so a pageable C (whose
+// copies return only when done) still overlaps the remaining panels.
+template <class PanelFn>
+gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
+                            void *C, int ab_bytes, int c_bytes, void *dA, void *dB, void *dC, PanelFn panel)
+{
+    const int64_t rows = gemmpipe_host_panel_rows(M);
+    const int64_t P = (M + rows - 1) / rows;
+    HostPipe h;
+    gemmpipe_status_t st = host_pipe(dev, s, static_cast<size_t>(2 * P + 4), &h);
+    if (st != GEMMPIPE_OK) return st;
+    cudaEvent_t *ev = h.ev.data();  // [0] start, [1] B in, [2, 2+P) A panels in, [2+P, 2+2P) panels done,
+                                    // [2+2P] all in, [3+2P] all out
+    const auto ok = [](cudaError_t e) {
+        if (e == cudaSuccess) return true;
+        cudaGetLastError();
+        return false;
+    };
+    if (!ok(cudaEventRecord(ev[0], s)) || !ok(cudaStreamWaitEvent(h.in, ev[0], 0)) ||
+        !ok(cudaStreamWaitEvent(h.out, ev[0], 0)))
+        return GEMMPIPE_ERR_LAUNCH;
+    const char *hA = static_cast<const char *>(A);
+    char *dAc = static_cast<char *>(dA);
+    char *dCc = static_cast<char *>(dC);
+    char *hC = static_cast<char *>(C);
+    bool good = true;
+    if (K > 0) {
+        good = ok(cudaMemcpyAsync(dB, B, static_cast<size_t>(K * N * ab_bytes), cudaMemcpyDefault, h.in)) &&
+               ok(cudaEventRecord(ev[1], h.in));
+        for (int64_t p = 0; good && p < P; ++p) {
+            const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
+            good = ok(cudaMemcpyAsync(dAc + r0 * K * ab_bytes, hA + r0 * K * ab_bytes,
+                                      static_cast<size_t>(mp * K * ab_bytes), cudaMemcpyDefault, h.in)) &&
+                   ok(cudaEventRecord(ev[2 + p], h.in));
+        }
+    }
+    if (good && K > 0) good = ok(cudaStreamWaitEvent(s, ev[1], 0));
+    for (int64_t p = 0; good && p < P; ++p) {
+        const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
+        if (K > 0 && !ok(cudaStreamWaitEvent(s, ev[2 + p], 0))) {
+            good = false;
+            break;
+        }
+        if ((st = panel(r0, mp)) != GEMMPIPE_OK) break;
+        good = ok(cudaEventRecord(ev[2 + P + p], s));
+    }
+    if (good && st == GEMMPIPE_OK) {
+        for (int64_t p = 0; good && p < P; ++p) {
+            const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
+            good = ok(cudaStreamWaitEvent(h.out, ev[2 + P + p], 0)) &&
+                   ok(cudaMemcpyAsync(hC + r0 * N * c_bytes, dCc + r0 * N * c_bytes,
+                                      static_cast<size_t>(mp * N * c_bytes), cudaMemcpyDefault, h.out));
+        }
+    }
+    // Whatever was enqueued, the caller's stream ends after both side
+    // streams, so later work on it never races these copies.
+    const bool joined = ok(cudaEventRecord(ev[2 + 2 * P], h.in)) && ok(cudaEventRecord(ev[3 + 2 * P], h.out)) &&
+                        ok(cudaStreamWaitEvent(s, ev[2 + 2 * P], 0)) && ok(cudaStreamWaitEvent(s, ev[3 + 2 * P], 0));
+    if (st != GEMMPIPE_OK) return st;
+    return good && joined ? GEMMPIPE_OK : GEMMPIPE_ERR_LAUNCH;
+}
+
+// Device buffers of a host-buffer call: A, B and C, each 256-byte aligned.
+gemmpipe_status_t host_buffers(int dev, cudaStream_t s, int64_t M, int64_t N, int64_t K, int ab_bytes, int c_bytes,
+                               void **dA, void **dB, void **dC)
+{
+    const int64_t a = align256(M * K * ab_bytes), b = align256(K * N * ab_bytes), c = M * N * c_bytes;
+    void *ws = nullptr;
+    gemmpipe_status_t st = workspace(dev, s, a + b + c, &ws, kWsHost);
+    if (st != GEMMPIPE_OK) return st;
+    *dA = ws;
+    *dB = static_cast<char *>(ws) + a;
+    *dC = static_cast<char *>(ws) + a + b;
+    return GEMMPIPE_OK;
+}
+
+}  // namespace
+
 extern "C" {
+
+int64_t gemmpipe_host_panel_rows(int64_t M)
+{
+    if (M <= 0) return 512;
+    int64_t r = (M + 7) / 8;
+    r = (r + 255) / 256 * 256;
+    return r < 512 ? 512 : r;
+}
+
+gemmpipe_status_t gemm_s8s8s32_host(int64_t M, int64_t N, int64_t K, const int8_t *A, const int8_t *B, int32_t *C,
+                                    gemmpipe_stream_t stream)
+{
+    gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 1, 4);
+    if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceInfo d;
+    if ((st = device_info(&d, &dev)) != GEMMPIPE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+    if ((st = host_buffers(dev, s, M, N, K, 1, 4, &dA, &dB, &dC)) != GEMMPIPE_OK) return st;
+    const int8_t *A8 = static_cast<const int8_t *>(dA), *B8 = static_cast<const int8_t *>(dB);
+    int32_t *C32 = static_cast<int32_t *>(dC);
+    // B is widened once; each panel widens its rows of A into their place
+    // in the operand workspace and runs the GEMM on them.  Plans that do not
+    // use widened copies (the comparison path, in-kernel widening) and K = 0
+    // go through gemm_s8s8s32 per panel.
+    const bool direct = K == 0 || imma_wanted(A8, K) || s8_convert_ok(A8, K, B8, N);
+    const int64_t Kp = round8(K), Np = round8(N);
+    uint16_t *A16 = nullptr, *B16 = nullptr;
+    bool b_ready = false;
+    if (!direct) {
+        void *ws = nullptr;
+        if ((st = workspace(dev, s, s8_workspace_bytes(M, N, K), &ws)) != GEMMPIPE_OK) return st;
+        A16 = static_cast<uint16_t *>(ws);
+        B16 = A16 + M * Kp;
+    }
+    auto widen = [&](const int8_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch) {
+        TimedRegion tr(false, s);
+        const cudaError_t e = gp::launch_widen_s8_f16(src, rows, cols, dst, pitch, src, 0, cols, dst, pitch, d.sms, s);
+        tr.end();
+        if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
+        g_launches.fetch_add(1);
+        return GEMMPIPE_OK;
+    };
+    return host_call(dev, s, M, N, K, A, B, C, 1, 4, dA, dB, dC, [&](int64_t r0, int64_t mp) {
+        if (direct) return gemm_s8s8s32(mp, N, K, A8 + r0 * K, B8, C32 + r0 * N, stream);
+        gemmpipe_status_t e;
+        if (!b_ready) {
+            if ((e = widen(B8, K, N, B16, Np)) != GEMMPIPE_OK) return e;
+            b_ready = true;
+        }
+        if ((e = widen(A8 + r0 * K, mp, K, A16 + r0 * Kp, Kp)) != GEMMPIPE_OK) return e;
+        Plan pl;
+        if ((e = make_plan(true, mp, N, K, A16 + r0 * Kp, Kp, B16, Np, C32 + r0 * N, N, d, &pl)) != GEMMPIPE_OK)
+            return e;
+        return run_plan(pl, dev, mp, N, K, A16 + r0 * Kp, Kp, B16, Np, C32 + r0 * N, N, s);
+    });
+}
+
+gemmpipe_status_t gemm_f16f32_host(int64_t M, int64_t N, int64_t K, const gemmpipe_half_t *A,
+                                   const gemmpipe_half_t *B, float *C, gemmpipe_stream_t stream)
+{
+    gemmpipe_status_t st = check_shape(M, N, K, A, B, C, 2, 4);
+    if (st != GEMMPIPE_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceInfo d;
+    if ((st = device_info(&d, &dev)) != GEMMPIPE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+    if ((st = host_buffers(dev, s, M, N, K, 2, 4, &dA, &dB, &dC)) != GEMMPIPE_OK) return st;
+    const gemmpipe_half_t *A16 = static_cast<const gemmpipe_half_t *>(dA);
+    const gemmpipe_half_t *B16 = static_cast<const gemmpipe_half_t *>(dB);
+    float *C32 = static_cast<float *>(dC);
+    return host_call(dev, s, M, N, K, A, B, C, 2, 4, dA, dB, dC, [&](int64_t r0, int64_t mp) {
+        return gemm_f16f32(mp, N, K, A16 + r0 * K, B16, C32 + r0 * N, stream);
+    });
+}
+
 
 gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K, const gemmpipe_half_t *A, const gemmpipe_half_t *B,
                               float *C, gemmpipe_stream_t stream)
@@ -921,6 +1122,13 @@ gemmpipe_status_t gemmpipe_release_workspaces(void)
         }
     }
     g_ws.clear();
+    for (auto &kv : g_host) {
+        cudaSetDevice(kv.first.first);
+        if (kv.second.in) cudaStreamDestroy(kv.second.in);
+        if (kv.second.out) cudaStreamDestroy(kv.second.out);
+        for (cudaEvent_t e : kv.second.ev) cudaEventDestroy(e);
+    }
+    g_host.clear();
     if (have) cudaSetDevice(cur);
     cudaGetLastError();
     return GEMMPIPE_OK;

@@ -56,6 +56,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gemm_s8s8s32": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemm_f16f32": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemm_s8s8s32_noalloc": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+        "gemm_s8s8s32_host": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+        "gemm_f16f32_host": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+        "gemmpipe_host_panel_rows": (_i64, [_i64]),
         "gemmpipe_get_device_status": (_int, [_vp]),
         "gemmpipe_status_string": (ctypes.c_char_p, [_int]),
         "gemmpipe_compute_load_ratio": (ctypes.c_double, [_int, _int, _int, _int]),
@@ -91,6 +94,8 @@ def _ptr(x) -> int | None:
         return x
     if hasattr(x, "data_ptr"):
         return int(x.data_ptr())
+    if hasattr(x, "__array_interface__"):
+        return int(x.__array_interface__["data"][0])
     raise TypeError(f"expected a tensor or an address, got {type(x)!r}")
 
 
@@ -124,6 +129,24 @@ def gemm_s8s8s32_noalloc(M, N, K, A, B, C, stream=None) -> None:
     needing more are refused; calls overlapping on the GPU race on it."""
     _check(load().gemm_s8s8s32_noalloc(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)),
            "gemm_s8s8s32_noalloc")
+
+
+def gemm_s8s8s32_host(M, N, K, A, B, C, stream=None) -> None:
+    """gemm_s8s8s32 with A, B and C in host memory (CPU tensors or numpy
+    arrays): copies in, GEMM and copies out overlapped by row panels.
+    Asynchronous for page-locked buffers: synchronize `stream` before
+    reading C."""
+    _check(load().gemm_s8s8s32_host(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_s8s8s32_host")
+
+
+def gemm_f16f32_host(M, N, K, A, B, C, stream=None) -> None:
+    """gemm_f16f32 with A, B and C in host memory (see gemm_s8s8s32_host)."""
+    _check(load().gemm_f16f32_host(M, N, K, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "gemm_f16f32_host")
+
+
+def gemmpipe_host_panel_rows(M: int) -> int:
+    """Rows per panel of the host-buffer calls (no GPU needed)."""
+    return int(load().gemmpipe_host_panel_rows(M))
 
 
 def gemmpipe_get_device_status(stream=None) -> int:

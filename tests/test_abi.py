@@ -77,6 +77,26 @@ def test_host_side_argument_checks(lib):
     assert lib.gemmpipe_test_inject_stall(3, 0) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_test_inject_stall(-1, 0) == gemmpipe.OK
     assert lib.gemmpipe_copy(None, None, -1, None) == gemmpipe.ERR_INVALID_VALUE
+    # Host-buffer calls: the same checks, before any device call.
+    for fn in (lib.gemm_s8s8s32_host, lib.gemm_f16f32_host):
+        assert fn(-1, 4, 4, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
+        assert fn(4, 4, 4, fake, fake, None, None) == gemmpipe.ERR_INVALID_VALUE
+        assert fn(4, 4, 4, fake, fake, fake + 2, None) == gemmpipe.ERR_INVALID_VALUE  # C misaligned
+        assert fn(big, 8, big, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
+        assert fn(0, 4, 4, None, None, None, None) == gemmpipe.OK
+    assert lib.gemm_f16f32_host(4, 4, 4, fake + 1, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
+
+
+def test_host_panel_rows(lib):
+    rows = gemmpipe.gemmpipe_host_panel_rows
+    # At least 512 rows; about M / 8 rounded up to 256 beyond that.
+    assert [rows(m) for m in (0, 1, 512, 513, 4096, 4097, 8192, 16384, 100000)] == \
+        [512, 512, 512, 512, 512, 768, 1024, 2048, 12544]
+    for m in range(1, 20000, 97):
+        r = rows(m)
+        assert r % 256 == 0 and r >= 512
+        panels = -(-m // r)
+        assert panels <= 8 and (panels == 1 or r * (panels - 1) < m)
 
 
 def test_no_gpu_fails_loudly(lib):
@@ -89,6 +109,8 @@ def test_no_gpu_fails_loudly(lib):
     assert lib.gemm_s8s8s32(8, 8, 8, fake, fake, fake, None) == gemmpipe.ERR_UNSUPPORTED_DEVICE
     with pytest.raises(gemmpipe.GemmpipeError):
         gemmpipe.gemm_f16f32(8, 8, 8, fake, fake, fake, stream=0)
+    assert lib.gemm_s8s8s32_host(8, 8, 8, fake, fake, fake, None) == gemmpipe.ERR_UNSUPPORTED_DEVICE
+    assert lib.gemm_f16f32_host(8, 8, 8, fake, fake, fake, None) == gemmpipe.ERR_UNSUPPORTED_DEVICE
 
 
 def test_header_parses():
