@@ -47,9 +47,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # hash as they did when the counters were taken.
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu"]
 TRAFFIC = {
-    # (int8 operands, cta pair, BN): (bytes per launch, sources hash, profile)
-    ("s8", 1, 256): (138_815_232, "61e6ac4fb09ee2ce", "profiles/gemm_pair_int8_4096.md"),
-    ("f16", 1, 256): (140_950_784, "61e6ac4fb09ee2ce", "profiles/gemm_pair_f16_4096.md"),
+    # (dtype, M, N, K, cta pair, BN): (bytes per launch, sources hash, profile)
+    ("s8", 4096, 4096, 4096, 1, 256): (138_815_232, "61e6ac4fb09ee2ce", "profiles/gemm_pair_int8_4096.md"),
+    ("f16", 4096, 4096, 4096, 1, 256): (140_950_784, "61e6ac4fb09ee2ce", "profiles/gemm_pair_f16_4096.md"),
+    ("f16", 16384, 128, 16384, 0, 128): (545_099_776, "61e6ac4fb09ee2ce", "profiles/gemm_skinny_f16_16384x128x16384.md"),
+    ("f16", 4093, 3001, 4107, 1, 256): (114_701_568, "61e6ac4fb09ee2ce", "profiles/gemm_pair_f16_ragged_4093x3001x4107.md"),
 }
 
 
@@ -63,10 +65,8 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(dtype: str, plan: dict, shape: tuple) -> tuple[int | None, str | None]:
-    """Captured DRAM traffic of the 4096^3 launch this plan runs, or None."""
-    if shape != (4096, 4096, 4096):
-        return None, None
-    t = TRAFFIC.get((dtype, plan["cta_pair"], plan["BN"]))
+    """Captured DRAM traffic of the launch this plan runs on this shape, or None."""
+    t = TRAFFIC.get((dtype, *shape, plan["cta_pair"], plan["BN"]))
     if t is None or t[1] != kernel_source_hash():
         return None, None
     return t[0], t[2]
@@ -269,8 +269,11 @@ def measure_gemm(wl, steps: int, warmup: int, dev, flush, peaks, peak_src):
     if skinny:
         peak = peaks["hbm_gbs"]
         achieved = alg_bytes / kernel_ms / 1e6
+        traffic, prof = measured_traffic(dtype, plan, (M, N, K))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": f"hbm_gbs ({peak_src})"}
+                "traffic": traffic, "peak_source": f"hbm_gbs ({peak_src})"}
+        if prof:
+            roof["traffic_source"] = prof
         roof["kernel_timing"] = KERNEL_TIMING
     else:
         peak = peaks["bf16_tflops"]
@@ -392,11 +395,11 @@ def run_gpu(args) -> int:
     # charged to the timed step).
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int32, device=dev)
 
     def flush():
         flush_buf.zero_()
-        torch.sum(clean_buf, dim=0, dtype=torch.int64, out=flush_sink)
+        torch.sum(clean_buf, dim=0, dtype=torch.int32, out=flush_sink)  # int32 in and out: a read, no cast
 
     clock = ClockSampler(local)
     clock.start()
@@ -523,11 +526,11 @@ def run_ablation(args) -> int:
     torch.cuda.set_device(dev)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    sink = torch.empty((), dtype=torch.int64, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
 
     def flush():
         flush_buf.zero_()
-        torch.sum(clean_buf, dim=0, dtype=torch.int64, out=sink)
+        torch.sum(clean_buf, dim=0, dtype=torch.int32, out=sink)
 
     ops = {}
     rows = []
