@@ -32,15 +32,17 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi)
 struct WidenJob {
     const int8_t *src;
     int64_t rows, cols;
+    int64_t spitch;  // source row pitch in elements (>= cols)
     uint16_t *dst;
     int64_t pitch;  // destination row pitch in elements, a multiple of 8
+    int64_t dcols;  // destination columns written (>= cols, a multiple of 8; past cols: zeros)
 };
 
 // Loads the 16 int8 of one piece of row r (one 16-byte load when the row
 // is 16-byte aligned and the piece whole, else byte loads of the valid ones).
 __device__ __forceinline__ uint4 widen_load(const WidenJob &j, int64_t r, int64_t c)
 {
-    const int8_t *src = j.src + r * j.cols + c;
+    const int8_t *src = j.src + r * j.spitch + c;
     const int64_t valid = j.cols - c;
     if (valid >= 16 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
         return __ldg(reinterpret_cast<const uint4 *>(src));
@@ -77,7 +79,7 @@ __device__ __forceinline__ void widen_store(const WidenJob &j, int64_t r, int64_
     }
     uint16_t *dst = j.dst + r * j.pitch + c;
     reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    if (j.pitch - c > 8) reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (j.dcols - c > 8) reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // blockIdx.z picks the matrix (0: A, 1: B); x covers 16-element pieces of a
@@ -92,7 +94,7 @@ __global__ void widen_s8_f16_kernel(const WidenJob ja, const WidenJob jb)
     pdl_launch_dependents();
     const WidenJob &j = blockIdx.z == 0 ? ja : jb;
     const int64_t c = 16 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
-    if (c >= j.pitch) return;
+    if (c >= j.dcols) return;
     const int64_t step = gridDim.y;
     for (int64_t r = blockIdx.y; r < j.rows; r += kRowBatch * step) {
         uint4 v[kRowBatch];
@@ -531,6 +533,8 @@ int resident_blocks(K k, int threads)
     return n;
 }
 
+cudaError_t launch_widen_jobs(const WidenJob &ja, const WidenJob &jb, int sms, cudaStream_t s);
+
 cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16, int64_t pitchA,
                                 const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB,
                                 int sms, cudaStream_t s)
@@ -570,10 +574,22 @@ cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, u
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    const WidenJob ja{A, rowsA, colsA, A16, pitchA};
-    const WidenJob jb{B, rowsB, colsB, B16, pitchB};
+    return launch_widen_jobs(WidenJob{A, rowsA, colsA, colsA, A16, pitchA, pitchA},
+                             WidenJob{B, rowsB, colsB, colsB, B16, pitchB, pitchB}, sms, s);
+}
+
+cudaError_t launch_widen_s8_f16_cols(const int8_t *src, int64_t rows, int64_t cols, int64_t spitch, uint16_t *dst,
+                                     int64_t dpitch, int sms, cudaStream_t s)
+{
+    const WidenJob j{src, rows, cols, spitch, dst, dpitch, (cols + 7) / 8 * 8};
+    return launch_widen_jobs(j, WidenJob{src, 0, cols, spitch, dst, dpitch, j.dcols}, sms, s);
+}
+
+cudaError_t launch_widen_jobs(const WidenJob &ja, const WidenJob &jb, int sms, cudaStream_t s)
+{
+    const int64_t rowsA = ja.rows, rowsB = jb.rows;
     const int threads = 128;
-    const int64_t maxpitch = pitchA > pitchB ? pitchA : pitchB;
+    const int64_t maxpitch = ja.dcols > jb.dcols ? ja.dcols : jb.dcols;
     const int64_t gx = ((maxpitch + 15) / 16 + threads - 1) / threads;
     const int64_t maxrows = rowsA > rowsB ? rowsA : rowsB;
     // One resident wave of blocks over both matrices, and at least a whole

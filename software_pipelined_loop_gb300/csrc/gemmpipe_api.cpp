@@ -693,20 +693,30 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 // One host-buffer call: B and the row panels of A go to device buffers on
 // the `in` stream, panel p's GEMM runs on the caller's stream once its rows
 // have arrived, and its rows of C go back on the `out` stream while later
-// panels compute.  `panel` enqueues the kernels of rows [r0, r0 + rows).
+// panels compute.  With `split_cols` > 0 the first panel is computed in two
+// column halves, [0, split_cols) and the rest: B comes in those halves
+// (first panel's rows of A before them), so the first C values start back
+// after half of B instead of all of it.  `prep_b(c0, nc)` enqueues what B's
+// columns [c0, c0 + nc) need once they have arrived; `panel(r0, mp, c0, nc)`
+// enqueues the kernels of C's rows [r0, r0 + mp) x columns [c0, c0 + nc).
 // Everything is enqueued before the first copy back, so a pageable C (whose
 // copies return only when done) still overlaps the remaining panels.
-template <class PanelFn>
+template <class PrepFn, class PanelFn>
 gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
-                            void *C, int ab_bytes, int c_bytes, void *dA, void *dB, void *dC, PanelFn panel)
+                            void *C, int ab_bytes, int c_bytes, void *dA, void *dB, void *dC, int64_t split_cols,
+                            PrepFn prep_b, PanelFn panel)
 {
     const int64_t rows = gemmpipe_host_panel_rows(M);
     const int64_t P = (M + rows - 1) / rows;
+    const bool split = split_cols > 0 && split_cols < N && K > 0;
     HostPipe h;
-    gemmpipe_status_t st = host_pipe(dev, s, static_cast<size_t>(2 * P + 4), &h);
+    gemmpipe_status_t st = host_pipe(dev, s, static_cast<size_t>(2 * P + 6), &h);
     if (st != GEMMPIPE_OK) return st;
-    cudaEvent_t *ev = h.ev.data();  // [0] start, [1] B in, [2, 2+P) A panels in, [2+P, 2+2P) panels done,
-                                    // [2+2P] all in, [3+2P] all out
+    // Events: [0] start, [1] B (or its first half) in, [2] B's second half
+    // in, [3, 3+P) A panels in, [3+P] first panel's first half done,
+    // [4+P, 4+2P) panels done, [4+2P] all in, [5+2P] all out.
+    cudaEvent_t *ev = h.ev.data();
+    cudaEvent_t *ev_a = ev + 3, *ev_c = ev + 4 + P;
     const auto ok = [](cudaError_t e) {
         if (e == cudaSuccess) return true;
         cudaGetLastError();
@@ -716,44 +726,91 @@ gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64
         !ok(cudaStreamWaitEvent(h.out, ev[0], 0)))
         return GEMMPIPE_ERR_LAUNCH;
     const char *hA = static_cast<const char *>(A);
+    const char *hB = static_cast<const char *>(B);
     char *dAc = static_cast<char *>(dA);
+    char *dBc = static_cast<char *>(dB);
     char *dCc = static_cast<char *>(dC);
     char *hC = static_cast<char *>(C);
+    const size_t brow = static_cast<size_t>(N * ab_bytes), crow = static_cast<size_t>(N * c_bytes);
+    auto rows_of = [&](int64_t p) { return M - p * rows < rows ? M - p * rows : rows; };
+    auto copy_a = [&](int64_t p) {
+        const int64_t r0 = p * rows;
+        return ok(cudaMemcpyAsync(dAc + r0 * K * ab_bytes, hA + r0 * K * ab_bytes,
+                                  static_cast<size_t>(rows_of(p) * K * ab_bytes), cudaMemcpyDefault, h.in)) &&
+               ok(cudaEventRecord(ev_a[p], h.in));
+    };
+    // B's columns [c0, c0 + nc) in, as a 2-D copy (whole rows: one copy).
+    auto copy_b = [&](int64_t c0, int64_t nc) {
+        if (nc == N)
+            return ok(cudaMemcpyAsync(dB, B, static_cast<size_t>(K) * brow, cudaMemcpyDefault, h.in));
+        return ok(cudaMemcpy2DAsync(dBc + c0 * ab_bytes, brow, hB + c0 * ab_bytes, brow,
+                                    static_cast<size_t>(nc * ab_bytes), static_cast<size_t>(K), cudaMemcpyDefault,
+                                    h.in));
+    };
     bool good = true;
     if (K > 0) {
-        good = ok(cudaMemcpyAsync(dB, B, static_cast<size_t>(K * N * ab_bytes), cudaMemcpyDefault, h.in)) &&
-               ok(cudaEventRecord(ev[1], h.in));
-        for (int64_t p = 0; good && p < P; ++p) {
-            const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
-            good = ok(cudaMemcpyAsync(dAc + r0 * K * ab_bytes, hA + r0 * K * ab_bytes,
-                                      static_cast<size_t>(mp * K * ab_bytes), cudaMemcpyDefault, h.in)) &&
-                   ok(cudaEventRecord(ev[2 + p], h.in));
+        if (split) {
+            good = copy_a(0) && copy_b(0, split_cols) && ok(cudaEventRecord(ev[1], h.in)) &&
+                   copy_b(split_cols, N - split_cols) && ok(cudaEventRecord(ev[2], h.in));
+            for (int64_t p = 1; good && p < P; ++p) good = copy_a(p);
+        } else {
+            good = copy_b(0, N) && ok(cudaEventRecord(ev[1], h.in));
+            for (int64_t p = 0; good && p < P; ++p) good = copy_a(p);
         }
     }
-    if (good && K > 0) good = ok(cudaStreamWaitEvent(s, ev[1], 0));
-    for (int64_t p = 0; good && p < P; ++p) {
-        const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
-        if (K > 0 && !ok(cudaStreamWaitEvent(s, ev[2 + p], 0))) {
-            good = false;
-            break;
+    auto wait = [&](cudaEvent_t e) { return K == 0 || ok(cudaStreamWaitEvent(s, e, 0)); };
+    if (good) {
+        if (split) {
+            good = wait(ev_a[0]) && wait(ev[1]);
+            if (good && (st = prep_b(0, split_cols)) == GEMMPIPE_OK && (st = panel(0, rows_of(0), 0, split_cols)) ==
+                                                                            GEMMPIPE_OK) {
+                good = ok(cudaEventRecord(ev[3 + P], s)) && wait(ev[2]);
+                if (good && (st = prep_b(split_cols, N - split_cols)) == GEMMPIPE_OK &&
+                    (st = panel(0, rows_of(0), split_cols, N - split_cols)) == GEMMPIPE_OK)
+                    good = ok(cudaEventRecord(ev_c[0], s));
+            }
+        } else {
+            good = wait(ev[1]) && wait(ev_a[0]);
+            if (good && (st = prep_b(0, N)) == GEMMPIPE_OK && (st = panel(0, rows_of(0), 0, N)) == GEMMPIPE_OK)
+                good = ok(cudaEventRecord(ev_c[0], s));
         }
-        if ((st = panel(r0, mp)) != GEMMPIPE_OK) break;
-        good = ok(cudaEventRecord(ev[2 + P + p], s));
+    }
+    for (int64_t p = 1; good && st == GEMMPIPE_OK && p < P; ++p) {
+        good = wait(ev_a[p]);
+        if (good && (st = panel(p * rows, rows_of(p), 0, N)) == GEMMPIPE_OK) good = ok(cudaEventRecord(ev_c[p], s));
     }
     if (good && st == GEMMPIPE_OK) {
-        for (int64_t p = 0; good && p < P; ++p) {
-            const int64_t r0 = p * rows, mp = (M - r0 < rows) ? M - r0 : rows;
-            good = ok(cudaStreamWaitEvent(h.out, ev[2 + P + p], 0)) &&
-                   ok(cudaMemcpyAsync(hC + r0 * N * c_bytes, dCc + r0 * N * c_bytes,
-                                      static_cast<size_t>(mp * N * c_bytes), cudaMemcpyDefault, h.out));
+        if (split) {
+            const size_t r = static_cast<size_t>(rows_of(0));
+            good = ok(cudaStreamWaitEvent(h.out, ev[3 + P], 0)) &&
+                   ok(cudaMemcpy2DAsync(hC, crow, dCc, crow, static_cast<size_t>(split_cols * c_bytes), r,
+                                        cudaMemcpyDefault, h.out)) &&
+                   ok(cudaStreamWaitEvent(h.out, ev_c[0], 0)) &&
+                   ok(cudaMemcpy2DAsync(hC + split_cols * c_bytes, crow, dCc + split_cols * c_bytes, crow,
+                                        static_cast<size_t>((N - split_cols) * c_bytes), r, cudaMemcpyDefault,
+                                        h.out));
+        }
+        for (int64_t p = split ? 1 : 0; good && p < P; ++p) {
+            const int64_t r0 = p * rows;
+            good = ok(cudaStreamWaitEvent(h.out, ev_c[p], 0)) &&
+                   ok(cudaMemcpyAsync(hC + r0 * crow, dCc + r0 * crow, static_cast<size_t>(rows_of(p)) * crow,
+                                      cudaMemcpyDefault, h.out));
         }
     }
     // Whatever was enqueued, the caller's stream ends after both side
     // streams, so later work on it never races these copies.
-    const bool joined = ok(cudaEventRecord(ev[2 + 2 * P], h.in)) && ok(cudaEventRecord(ev[3 + 2 * P], h.out)) &&
-                        ok(cudaStreamWaitEvent(s, ev[2 + 2 * P], 0)) && ok(cudaStreamWaitEvent(s, ev[3 + 2 * P], 0));
+    const bool joined = ok(cudaEventRecord(ev[4 + 2 * P], h.in)) && ok(cudaEventRecord(ev[5 + 2 * P], h.out)) &&
+                        ok(cudaStreamWaitEvent(s, ev[4 + 2 * P], 0)) && ok(cudaStreamWaitEvent(s, ev[5 + 2 * P], 0));
     if (st != GEMMPIPE_OK) return st;
     return good && joined ? GEMMPIPE_OK : GEMMPIPE_ERR_LAUNCH;
+}
+
+// Columns of the first panel's first half when splitting pays: B of at least
+// 4 MiB, and halves that keep every TMA base and pitch on 16 bytes.
+int64_t host_split_cols(int64_t N, int64_t K, int ab_bytes)
+{
+    if (N % 32 != 0 || N < 512 || K * N * ab_bytes < (int64_t(4) << 20)) return 0;
+    return N / 2 / 16 * 16;
 }
 
 // Device buffers of a host-buffer call: A, B and C, each 256-byte aligned.
@@ -802,33 +859,44 @@ gemmpipe_status_t gemm_s8s8s32_host(int64_t M, int64_t N, int64_t K, const int8_
     const bool direct = K == 0 || imma_wanted(A8, K) || s8_convert_ok(A8, K, B8, N);
     const int64_t Kp = round8(K), Np = round8(N);
     uint16_t *A16 = nullptr, *B16 = nullptr;
-    bool b_ready = false;
     if (!direct) {
         void *ws = nullptr;
         if ((st = workspace(dev, s, s8_workspace_bytes(M, N, K), &ws)) != GEMMPIPE_OK) return st;
         A16 = static_cast<uint16_t *>(ws);
         B16 = A16 + M * Kp;
     }
-    auto widen = [&](const int8_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t pitch) {
-        TimedRegion tr(false, s);
-        const cudaError_t e = gp::launch_widen_s8_f16(src, rows, cols, dst, pitch, src, 0, cols, dst, pitch, d.sms, s);
-        tr.end();
+    auto launched = [&](cudaError_t e) {
         if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
         g_launches.fetch_add(1);
         return GEMMPIPE_OK;
     };
-    return host_call(dev, s, M, N, K, A, B, C, 1, 4, dA, dB, dC, [&](int64_t r0, int64_t mp) {
+    // B's columns [c0, c0 + nc) into their place in the fp16 copy.
+    auto prep_b = [&](int64_t c0, int64_t nc) {
+        if (direct) return GEMMPIPE_OK;
+        TimedRegion tr(false, s);
+        const cudaError_t e =
+            nc == N ? gp::launch_widen_s8_f16(B8, K, N, B16, Np, B8, 0, N, B16, Np, d.sms, s)
+                    : gp::launch_widen_s8_f16_cols(B8 + c0, K, nc, N, B16 + c0, Np, d.sms, s);
+        tr.end();
+        return launched(e);
+    };
+    const int64_t split = direct ? 0 : host_split_cols(N, K, 1);
+    return host_call(dev, s, M, N, K, A, B, C, 1, 4, dA, dB, dC, split, prep_b,
+                     [&](int64_t r0, int64_t mp, int64_t c0, int64_t nc) {
         if (direct) return gemm_s8s8s32(mp, N, K, A8 + r0 * K, B8, C32 + r0 * N, stream);
         gemmpipe_status_t e;
-        if (!b_ready) {
-            if ((e = widen(B8, K, N, B16, Np)) != GEMMPIPE_OK) return e;
-            b_ready = true;
+        if (c0 == 0) {  // the panel's rows of A, once
+            TimedRegion tr(false, s);
+            const cudaError_t ce = gp::launch_widen_s8_f16(A8 + r0 * K, mp, K, A16 + r0 * Kp, Kp, A8 + r0 * K, 0, K,
+                                                           A16 + r0 * Kp, Kp, d.sms, s);
+            tr.end();
+            if ((e = launched(ce)) != GEMMPIPE_OK) return e;
         }
-        if ((e = widen(A8 + r0 * K, mp, K, A16 + r0 * Kp, Kp)) != GEMMPIPE_OK) return e;
         Plan pl;
-        if ((e = make_plan(true, mp, N, K, A16 + r0 * Kp, Kp, B16, Np, C32 + r0 * N, N, d, &pl)) != GEMMPIPE_OK)
+        if ((e = make_plan(true, mp, nc, K, A16 + r0 * Kp, Kp, B16 + c0, Np, C32 + r0 * N + c0, N, d, &pl)) !=
+            GEMMPIPE_OK)
             return e;
-        return run_plan(pl, dev, mp, N, K, A16 + r0 * Kp, Kp, B16, Np, C32 + r0 * N, N, s);
+        return run_plan(pl, dev, mp, nc, K, A16 + r0 * Kp, Kp, B16 + c0, Np, C32 + r0 * N + c0, N, s);
     });
 }
 
@@ -846,8 +914,18 @@ gemmpipe_status_t gemm_f16f32_host(int64_t M, int64_t N, int64_t K, const gemmpi
     const gemmpipe_half_t *A16 = static_cast<const gemmpipe_half_t *>(dA);
     const gemmpipe_half_t *B16 = static_cast<const gemmpipe_half_t *>(dB);
     float *C32 = static_cast<float *>(dC);
-    return host_call(dev, s, M, N, K, A, B, C, 2, 4, dA, dB, dC, [&](int64_t r0, int64_t mp) {
-        return gemm_f16f32(mp, N, K, A16 + r0 * K, B16, C32 + r0 * N, stream);
+    // The first panel's column halves run as plans on B's column slices,
+    // which needs TMA-describable operands (K a multiple of 8).
+    const int64_t split = K % 8 == 0 ? host_split_cols(N, K, 2) : 0;
+    return host_call(dev, s, M, N, K, A, B, C, 2, 4, dA, dB, dC, split,
+                     [](int64_t, int64_t) { return GEMMPIPE_OK; },
+                     [&](int64_t r0, int64_t mp, int64_t c0, int64_t nc) {
+        if (nc == N) return gemm_f16f32(mp, N, K, A16 + r0 * K, B16, C32 + r0 * N, stream);
+        Plan pl;
+        gemmpipe_status_t e;
+        const uint16_t *a = A16 + r0 * K, *b = B16 + c0;
+        if ((e = make_plan(false, mp, nc, K, a, K, b, N, C32 + r0 * N + c0, N, d, &pl)) != GEMMPIPE_OK) return e;
+        return run_plan(pl, dev, mp, nc, K, a, K, b, N, C32 + r0 * N + c0, N, s);
     });
 }
 

@@ -39,6 +39,11 @@ int variants_s8(const Variant **out);
 cudaError_t launch_widen_s8_f16(const int8_t *A, int64_t rowsA, int64_t colsA, uint16_t *A16, int64_t pitchA16,
                                 const int8_t *B, int64_t rowsB, int64_t colsB, uint16_t *B16, int64_t pitchB16,
                                 int sms, cudaStream_t s);
+// Widens columns [0, cols) of a rows x cols int8 block with source pitch
+// spitch into dst (pitch dpitch), writing only those columns (rounded up to
+// 8 with zeros): a column slice of a wider matrix.
+cudaError_t launch_widen_s8_f16_cols(const int8_t *src, int64_t rows, int64_t cols, int64_t spitch, uint16_t *dst,
+                                     int64_t dpitch, int sms, cudaStream_t s);
 cudaError_t launch_pad_f16(const uint16_t *src0, int64_t rows0, int64_t cols0, uint16_t *dst0, int64_t pitch0,
                            const uint16_t *src1, int64_t rows1, int64_t cols1, uint16_t *dst1, int64_t pitch1,
                            int sms, cudaStream_t s);
