@@ -183,11 +183,14 @@ GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32_noalloc(int64_t M, int64_t N, int64_
  * A, B and C are host pointers (any pointer cudaMemcpy accepts: pageable or
  * page-locked host memory, also managed or device memory).
  *
- * How: B is copied first, then A in row panels of gemmpipe_host_panel_rows(M)
- * rows, on a copy stream of the library's; panel p's GEMM runs on `stream`
- * as soon as its rows (and B) have arrived; its rows of C are copied back on
- * a second library stream while later panels compute.  The INT8 call
- * widens B once and each panel's rows of A as they arrive.
+ * How: A is copied in row panels of gemmpipe_host_panel_rows(M) rows, on a
+ * copy stream of the library's; panel p's GEMM runs on `stream` as soon as
+ * its rows and B have arrived; its rows of C are copied back on a second
+ * library stream while later panels compute.  The INT8 call widens B once
+ * and each panel's rows of A as they arrive.  When B holds at least 4 MiB
+ * and N is a multiple of 32, the first panel's rows go first and B follows
+ * in two column halves; the first panel is computed half by half, so C
+ * starts coming back after half of B.
  *
  * Ordering and completion: the copies start after all work enqueued on
  * `stream` before the call, and work enqueued on `stream` after the call
