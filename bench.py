@@ -12,7 +12,9 @@ CUDA events on its stream.
 
 Also measured in the same run and reported under ``secondary``: FP16
 4096^3 (TFLOPS), the skinny FP16 16384 x 128 x 16384 (GB/s of algorithmic
-bytes: A, B and C moved once) and the ragged FP16 4093 x 3001 x 4107.
+bytes: A, B and C moved once), the ragged FP16 4093 x 3001 x 4107, and the
+two small cases INT8 512^3 and FP16 1024^3 (launch- and latency-bound:
+reported, not targets).
 
 ``--impl reference`` times the CPU oracle on the host cores instead, on a
 bounded sample of rows of the same workload.
@@ -416,7 +418,7 @@ def run_gpu(args) -> int:
             clocks["window"] = "whole GPU phase (timed region shorter than the sampling period)"
         secondary = {}
         if not args.no_secondary:
-            for wl in (fp16_4096(), workload(3), workload(4)):
+            for wl in (fp16_4096(), workload(3), workload(4), workload(0), workload(1)):
                 r = measure_gemm(wl, max(10, args.steps // 4), args.warmup, dev, flush, peaks, peak_src)
                 secondary[r["name"]] = r
         e2e = measure_e2e(head, max(5, args.steps // 4), dev)
