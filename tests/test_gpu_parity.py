@@ -682,3 +682,18 @@ def test_c_beyond_2_31_elements(dev, dtype):
         np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B, rows=rows))
     else:
         assert_f16_close(got, oracle.gemm_f16f32(A, B, rows=rows))
+
+
+# ------------------------------------------------------ extreme aspect ratios
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("M,N,K", [(1, 65536, 64),      # one row, 256+ column tiles, split tail
+                                   (65536, 16, 32),     # tall and thin: 512 row tiles of a 128-wide variant
+                                   (2, 3, 200000),      # a single tile split over the whole grid
+                                   (128, 128, 131071)])  # the largest K whose int8 sums cannot wrap
+def test_extreme_aspect_ratios(dev, dtype, M, N, K):
+    A, B = inputs.make_operands(dtype, M, N, K, seed=2100 + M + N + K)
+    if dtype == "s8":
+        assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), f"{M}x{N}x{K}")
