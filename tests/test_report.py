@@ -116,3 +116,17 @@ def test_parse_raw_csv_and_bench_line(tmp_path):
     q = tmp_path / "raw.csv"
     q.write_text(csv_text)
     assert report.main(["--bench", str(p), "--ncu-csv", str(q)]) == 0
+
+
+def test_balance_points_match_the_pages_ga104_table():
+    # The page's worked example: GA104 peaks over 608 GB/s (tests/golden).
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "ga104_balance_points.json")))
+    for row in g["peaks"]:
+        L = report.Launch(name="ga104", dtype="f16", M=4096, N=4096, K=4096, kernel_ms=1.0, plan=dict(PAIR_PLAN),
+                          peak_tflops=row["peak_gflops"] / 1e3, peak_gbs=g["dram_gbs"])
+        r = report.roofline(L, report.baseline(L))
+        assert round(r["balance"], 1) == row["balance"], row["precision"]
+    # The page's effective-throughput formula at 4096^3 and 1 ms.
+    b = report.baseline(launch(kernel_ms=1.0))
+    assert b["tflops"] * 1e3 == pytest.approx(2 * 4096 ** 3 / (1.0 / 1000) / 1e9)
