@@ -34,9 +34,11 @@
  * allocated with cudaMalloc on first need, grown when a larger problem needs
  * it (cudaFree then waits for the device), released by
  * gemmpipe_release_workspaces() or at unload.  A second workspace per
- * (device, stream) holds stream-K partial sums: when the output tiles do not
- * divide evenly over the persistent grid, the k-blocks of the last waves'
- * tiles are split into equal ranges over all CTAs and a split tile's parts
+ * (device, stream) holds stream-K partial sums: when the output tiles leave
+ * the persistent grid's last wave at most 4/5 full (or, with fewer tiles
+ * than the grid holds, when spreading them cuts each CTA's k-blocks to a
+ * third or less), the k-blocks of the last waves' tiles are split into equal
+ * ranges over all CTAs and a split tile's parts
  * are added by the CTA holding its last k-block (128 x BN x 4 bytes per CTA
  * plus 64 KiB of flags; if it cannot be allocated, every tile runs whole
  * instead -- same result, no error).  gemm_f16f32 with 16-byte aligned operands and pitches
@@ -303,8 +305,10 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
  * 0 single CTAs, 1 CTA pairs where the shape allows them.  split: -1
  * automatic, 0 every tile whole (no stream-K split), 1 split wherever the
- * schedule can (also memory-bound shapes whose tiles already fill half the
- * grid).  Returns INVALID_VALUE for values outside these sets.
+ * schedule can (also where the automatic rule keeps whole tiles: a nearly
+ * full last wave, a modest cut in k-blocks per CTA, memory-bound shapes
+ * whose tiles already fill half the grid).  Returns INVALID_VALUE for values
+ * outside these sets.
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair,
                                                           int split);

@@ -246,11 +246,14 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
     // Persistent grid: at most one CTA (or CTA pair) per SM (pair) slot.
-    // Whole tiles go round-robin; when they leave a partial last wave, that
-    // wave and the one before it are spread over all units as equal ranges
-    // of k-blocks (stream-K), so every unit does the same work.  With fewer
-    // tiles than slots, all tiles are split over as many units as keep at
-    // least kMinSplitKb k-blocks each.
+    // Whole tiles go round-robin; when they leave a partial last wave that
+    // is at most 4/5 full, that wave and the one before it are spread over
+    // all units as equal ranges of k-blocks (stream-K), so every unit does
+    // the same work.  With fewer tiles than slots, all tiles are split over
+    // as many units as keep at least kMinSplitKb k-blocks each, when that
+    // cuts a unit's k-blocks to a third or less.  Measured on GB300: a
+    // split costs its fix-up and, with every SM streaming operands at once,
+    // a slower k-loop, so it pays only when the work per unit drops a lot.
     const int64_t slots = v->info.pair ? v->max_pairs() : d.sms;
     const int64_t T = pl->tiles;
     const bool split = split_ok && v->info.split_ok && ov.split != 0;
@@ -267,12 +270,13 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (split && T < slots) {
         const int64_t want = (T * pl->num_kb + kMinSplitKb - 1) / kMinSplitKb;
         const int64_t u = want < slots ? want : slots;
-        if (u > T && (ov.split == 1 || !(memory_bound && 2 * T >= slots))) {
+        if (u > T && (ov.split == 1 || (u >= 3 * T && !(memory_bound && 2 * T >= slots)))) {
             pl->units = u;
             pl->dp_tiles = 0;
             pl->sk_tiles = T;
         }
-    } else if (split && T > slots && T % slots != 0 && pl->num_kb > 1) {
+    } else if (split && T > slots && T % slots != 0 && pl->num_kb > 1 &&
+               (ov.split == 1 || 5 * (T % slots) <= 4 * slots)) {
         pl->sk_tiles = slots + T % slots;
         pl->dp_tiles = T - pl->sk_tiles;
     }

@@ -17,10 +17,12 @@ k-block counts, that
 * no unit has an empty range.
 
 The grid choice mirrors the library's planner: tiles < slots splits all
-tiles over min(slots, ceil(tiles * k_blocks / 8)) units when that is more
-than the tile count (unless the GEMM is memory-bound and its tiles already
-fill half the slots); more tiles than slots with a partial last wave split
-the last two waves' tiles (slots + tiles % slots) over all slots.
+tiles over u = min(slots, ceil(tiles * k_blocks / 8)) units when u is at
+least three times the tile count (unless the GEMM is memory-bound and its
+tiles already fill half the slots); more tiles than slots with a partial
+last wave at most 4/5 full split the last two waves' tiles (slots + tiles %
+slots) over all slots.  `force` is the plan override that splits wherever
+the schedule can.
 """
 from __future__ import annotations
 
@@ -31,13 +33,13 @@ import pytest
 MIN_SPLIT_KB = 8
 
 
-def plan(tiles: int, slots: int, num_kb: int, memory_bound: bool = False):
+def plan(tiles: int, slots: int, num_kb: int, memory_bound: bool = False, force: bool = False):
     units, dp_tiles, sk_tiles = min(tiles, slots), tiles, 0
     if tiles < slots:
         u = min(slots, -(-tiles * num_kb // MIN_SPLIT_KB))
-        if u > tiles and not (memory_bound and 2 * tiles >= slots):
+        if u > tiles and (force or (u >= 3 * tiles and not (memory_bound and 2 * tiles >= slots))):
             units, dp_tiles, sk_tiles = u, 0, tiles
-    elif tiles > slots and tiles % slots and num_kb > 1:
+    elif tiles > slots and tiles % slots and num_kb > 1 and (force or 5 * (tiles % slots) <= 4 * slots):
         sk_tiles = slots + tiles % slots
         dp_tiles = tiles - sk_tiles
     return units, dp_tiles, sk_tiles
@@ -79,10 +81,10 @@ CASES = [(t, g, k) for t, g, k in itertools.product(
     [1, 2, 3, 7, 8, 9, 64, 65, 256])]
 
 
-@pytest.mark.parametrize("memory_bound", [False, True], ids=["compute", "memory"])
+@pytest.mark.parametrize("mode", ["compute", "memory", "forced"])
 @pytest.mark.parametrize("tiles,slots,num_kb", CASES)
-def test_schedule_properties(tiles, slots, num_kb, memory_bound):
-    units, dp_tiles, sk_tiles = plan(tiles, slots, num_kb, memory_bound)
+def test_schedule_properties(tiles, slots, num_kb, mode):
+    units, dp_tiles, sk_tiles = plan(tiles, slots, num_kb, mode == "memory", mode == "forced")
     assert units <= slots and dp_tiles + sk_tiles == tiles
     sk_work = sk_tiles * num_kb
     if sk_tiles:
