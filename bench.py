@@ -178,11 +178,15 @@ def run_reference(args) -> int:
     if rank != 0:
         return 0
     name, dtype, M, N, K, A, B = workload(HEADLINE)
+    # Each step times a bounded sample of rows: about --ref-seconds of CPU
+    # work, less when many steps are asked for, so the whole run stays near
+    # two minutes.
+    per_step = args.ref_seconds if args.ref_seconds is not None else max(0.2, min(4.0, 120.0 / max(1, args.steps)))
     for _ in range(max(0, args.warmup)):
         cpu_oracle_rate(A, B, dtype, target_s=0.0, max_rows=8)
     vals, secs, rows, cores = [], 0.0, 0, 1
     for _ in range(max(1, args.steps)):
-        r = cpu_oracle_rate(A, B, dtype, target_s=args.ref_seconds)
+        r = cpu_oracle_rate(A, B, dtype, target_s=per_step)
         vals.append(r["value"])
         secs += r["seconds"]
         rows = r["rows"]
@@ -588,7 +592,8 @@ def main() -> int:
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--ref-seconds", type=float, default=None,
+                    help="CPU seconds per reference step (default: 4, or 120 / steps when that is less)")
     ap.add_argument("--shape", default=None,
                     help="time dtype,M,N,K (s8 or f16) as the headline instead of INT8 4096^3 "
                          "(for profiling and sweeps; uniform inputs)")
