@@ -353,6 +353,23 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_copy(void *dst, const void *src, int64_t
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int timeout_ms);
 
+/*
+ * Test hook that shows the pipelining ("Pipeline GPU Kernel", Steps 3-4:
+ * the loads of the next K-tiles are issued while the tensor cores work on
+ * this one).  For the next GEMM launch only, and when that launch runs the
+ * FP16 CTA-pair kernel with a 6- or 1-stage ring (the two kernels compiled
+ * with the trace; any other launch consumes the hook and records nothing),
+ * CTA 0 (the leader CTA of pair 0) writes %globaltimer nanoseconds into `buffer`, a
+ * device array of 2 * `entries` uint64: element j (j < entries) when its
+ * producer has issued the tile copies of its j-th k-block (counted over the
+ * CTA's whole schedule), element entries + j when its MMA thread finds that
+ * k-block's data ready, just before issuing its MMAs.  Elements past the
+ * CTA's k-blocks are left as they were.  entries = 0 clears the hook;
+ * entries above 2^20, or a buffer that is not device memory, give
+ * INVALID_VALUE.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_test_trace(void *buffer, int64_t entries);
+
 #ifdef __cplusplus
 }
 #endif

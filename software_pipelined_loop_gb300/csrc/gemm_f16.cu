@@ -16,6 +16,10 @@ static const Variant kF16Variants[] = {
     make_variant<GemmCfg<128, 6, false, false>>(),  // TMA producer, 128x128 tiles (N <= 128)
     make_variant<GemmCfg<256, 4, true, false>>(),   // bounded-load producer (misaligned inputs)
     make_variant<GemmCfg<128, 6, true, false>>(),
+    // Copies of the pair kernels at 6 and 1 stages that stamp the
+    // pipelining trace (taken only while the trace hook is armed).
+    make_variant<GemmCfg<256, 6, false, false, false, 1, true, 1, 4, true>>(),
+    make_variant<GemmCfg<256, 1, false, false, false, 1, true, 1, 4, true>>(),
 };
 
 int variants_f16(const Variant **out)

@@ -53,8 +53,11 @@ namespace gp {
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
 template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1,
-          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4>
+          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4, bool TRACE_ = false>
 struct GemmCfg {
+    // TRACE: a copy of the kernel that stamps the pipelining trace (the
+    // test hook gemmpipe_test_trace); the others carry no trace code.
+    static constexpr bool TRACE = TRACE_;
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
     static constexpr int BK = 64;  // 64 fp16 = 128 bytes = one swizzle-atom row
@@ -488,6 +491,9 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
                 tma_load_2d(sa, tA, fb, k0, m0);
 #pragma unroll
                 for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                if constexpr (Cfg::TRACE) {
+                    if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
+                }
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -674,6 +680,9 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 tma_load_2d_pair(sa, tA, fb, k0, m0);
 #pragma unroll
                 for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                if constexpr (Cfg::TRACE) {
+                    if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
+                }
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -719,6 +728,7 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
+    [[maybe_unused]] int64_t nkb = 0;  // k-blocks seen ready (trace copies only)
     WorkIter<Cfg> it(p);
     Work wk;
     while (ok && it.next(p, wk)) {
@@ -734,6 +744,10 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                 if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
                     ok = false;
                     break;
+                }
+                if constexpr (Cfg::TRACE) {
+                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) p.trace[p.trace_n + nkb] = globaltimer_ns();
+                    ++nkb;
                 }
                 tc_fence_after_sync();
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
@@ -782,6 +796,7 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
     bool issued = false, ok = true;
+    [[maybe_unused]] int64_t nkb = 0;  // k-blocks seen ready (trace copies only)
     WorkIter<Cfg> it(p);
     Work wk;
     while (ok && it.next(p, wk)) {
@@ -797,6 +812,10 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                 if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
                     ok = false;
                     break;
+                }
+                if constexpr (Cfg::TRACE) {
+                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) p.trace[p.trace_n + nkb] = globaltimer_ns();
+                    ++nkb;
                 }
                 tc_fence_after_sync();
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;

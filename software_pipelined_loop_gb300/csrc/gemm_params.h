@@ -37,6 +37,12 @@ struct GemmParams {
     int vec_store;         // C base and pitch allow 16-byte stores
     int tma_store;         // C blocks leave through TMA bulk-tensor stores (the C tensor map is valid)
     int64_t stall_kb;      // test hook: CTA 0 leaves this k-block unfilled (-1: none)
+    // Test hook: CTA 0 (the leader of pair 0) stamps %globaltimer into
+    // trace[j] when its producer has issued the copies of its j-th k-block
+    // and into trace[trace_n + j] when its MMA thread finds that k-block's
+    // data ready, for j < trace_n (nullptr: off).
+    unsigned long long *trace = nullptr;
+    int64_t trace_n = 0;
     uint64_t timeout_ns;   // bound of every pipeline wait
     int *status;           // device status word
 };

@@ -123,6 +123,12 @@ struct StallHook {
 };
 StallHook g_stall;
 
+struct TraceHook {
+    unsigned long long *buf = nullptr;
+    int64_t n = 0;
+};
+TraceHook g_trace_hook;
+
 struct Plan {
     const Variant *v = nullptr;
     int grid = 0;
@@ -174,8 +180,22 @@ const Variant *find_variant(int int_out, int convert, int producer, int bn, int 
     const int n = int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
     for (int i = 0; i < n; ++i) {
         const gp::VariantInfo &f = tab[i].info;
-        if (f.producer == producer && f.convert == convert && f.BN == bn && f.pair == pair &&
+        if (f.producer == producer && f.convert == convert && f.BN == bn && f.pair == pair && !f.traced &&
             (stages == 0 || f.stages == stages))
+            return &tab[i];
+    }
+    return nullptr;
+}
+
+// The trace-stamping copy of a variant, if one was compiled.
+const Variant *traced_twin(const Variant *v)
+{
+    const Variant *tab = nullptr;
+    const int n = v->info.int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
+    for (int i = 0; i < n; ++i) {
+        const gp::VariantInfo &f = tab[i].info;
+        if (f.traced && f.producer == v->info.producer && f.convert == v->info.convert && f.BN == v->info.BN &&
+            f.pair == v->info.pair && f.stages == v->info.stages && f.int_out == v->info.int_out)
             return &tab[i];
     }
     return nullptr;
@@ -519,6 +539,15 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
             p.stall_kb = g_stall.kb;
             p.timeout_ns = static_cast<uint64_t>(g_stall.timeout_ms) * 1000000ull;
             g_stall = StallHook();
+        }
+        if (g_trace_hook.buf) {
+            const Variant *tv = traced_twin(pl.v);
+            if (tv) {
+                pl.v = tv;
+                p.trace = g_trace_hook.buf;
+                p.trace_n = g_trace_hook.n;
+            }
+            g_trace_hook = TraceHook();
         }
     }
     if (gp::status_word(&p.status) != cudaSuccess) {
@@ -1267,6 +1296,22 @@ gemmpipe_status_t gemmpipe_copy(void *dst, const void *src, int64_t bytes, gemmp
     tr.end();
     if (e != cudaSuccess) return GEMMPIPE_ERR_LAUNCH;
     g_launches.fetch_add(1);
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_test_trace(void *buffer, int64_t entries)
+{
+    if (entries < 0 || entries > (int64_t(1) << 20)) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (entries == 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_trace_hook = TraceHook();
+        return GEMMPIPE_OK;
+    }
+    gemmpipe_status_t st = check_pointer(buffer, 8);
+    if (st != GEMMPIPE_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_trace_hook.buf = static_cast<unsigned long long *>(buffer);
+    g_trace_hook.n = entries;
     return GEMMPIPE_OK;
 }
 

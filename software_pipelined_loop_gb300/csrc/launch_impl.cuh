@@ -105,7 +105,7 @@ constexpr Variant make_variant()
 {
     return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::CONVERT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK,
                     Cfg::STAGES, Cfg::I8_STAGES, Cfg::PAIR ? 1 : 0, Cfg::THREADS, Cfg::SMEM_BYTES,
-                    Cfg::SUM_IN_C ? 0 : 1},
+                    Cfg::SUM_IN_C ? 0 : 1, Cfg::TRACE ? 1 : 0},
                    &launch_cfg<Cfg>, &max_pairs_cfg<Cfg>};
 }
 

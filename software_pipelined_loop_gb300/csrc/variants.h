@@ -19,6 +19,7 @@ struct VariantInfo {
     int threads;
     int smem_bytes;
     int split_ok;  // 1: the epilogue can take split (stream-K) tiles
+    int traced;    // 1: the copy that stamps the pipelining trace (test hook only)
 };
 
 using LaunchFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmParams &,

@@ -59,6 +59,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gemm_s8s8s32_host": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemm_f16f32_host": (_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
         "gemmpipe_host_panel_rows": (_i64, [_i64]),
+        "gemmpipe_test_trace": (_int, [_vp, _i64]),
         "gemmpipe_get_device_status": (_int, [_vp]),
         "gemmpipe_status_string": (ctypes.c_char_p, [_int]),
         "gemmpipe_compute_load_ratio": (ctypes.c_double, [_int, _int, _int, _int]),
@@ -201,6 +202,12 @@ def gemmpipe_launch_count() -> int:
 
 def gemmpipe_copy(dst, src, nbytes: int, stream=None) -> None:
     _check(load().gemmpipe_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "gemmpipe_copy")
+
+
+def gemmpipe_test_trace(buffer, entries: int) -> None:
+    """Arms the pipelining trace for the next GEMM launch (see the C header):
+    `buffer` is a device array of 2 * entries uint64."""
+    _check(load().gemmpipe_test_trace(_ptr(buffer), entries), "gemmpipe_test_trace")
 
 
 def gemmpipe_test_inject_stall(k_block: int, timeout_ms: int = 0) -> None:

@@ -77,6 +77,9 @@ def test_host_side_argument_checks(lib):
     assert lib.gemmpipe_test_inject_stall(3, 0) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_test_inject_stall(-1, 0) == gemmpipe.OK
     assert lib.gemmpipe_copy(None, None, -1, None) == gemmpipe.ERR_INVALID_VALUE
+    assert lib.gemmpipe_test_trace(None, -1) == gemmpipe.ERR_INVALID_VALUE
+    assert lib.gemmpipe_test_trace(fake, 1 << 21) == gemmpipe.ERR_INVALID_VALUE
+    assert lib.gemmpipe_test_trace(None, 0) == gemmpipe.OK
     # Host-buffer calls: the same checks, before any device call.
     for fn in (lib.gemm_s8s8s32_host, lib.gemm_f16f32_host):
         assert fn(-1, 4, 4, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
