@@ -661,6 +661,9 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     int64_t kb_count = 0;
     bool ok = true;
     constexpr uint32_t pair_bytes = 2u * Cfg::STAGE_BYTES;  // both CTAs' copies
+    const bool stall_cta = blockIdx.x == 0 && p.stall_kb >= 0;
+    const uint32_t full0 = smem_u32(&ctl->full[0]);
+    const uint32_t full0_leader = mapa_shared(full0, 0);
     WorkIter<Cfg> it(p);
     Work wk;
     while (ok && it.next(p, wk)) {
@@ -671,9 +674,9 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 ok = false;
                 break;
             }
-            if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) {
-                const uint32_t fb_local = smem_u32(&ctl->full[stage]);
-                const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's full[s]
+            if (!(stall_cta && kb_count == p.stall_kb)) {
+                const uint32_t fb_local = full0 + 8u * static_cast<uint32_t>(stage);
+                const uint32_t fb = full0_leader + 8u * static_cast<uint32_t>(stage);  // the leader's full[s]
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
@@ -724,6 +727,9 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
 {
     constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN, true);
     constexpr uint16_t BOTH = 3;
+    // Per-stage, per-k-step descriptors are offsets of these two (see mma_issuer).
+    const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);
+    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, 8192, 1024);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
@@ -750,14 +756,11 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                     ++nkb;
                 }
                 tc_fence_after_sync();
-                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
-                const uint32_t sb = sa + Cfg::A_BYTES;
+                const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
+                umma_f16_pair(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
-                    const uint64_t da = umma_desc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t db = umma_desc_sw128(sb + kk * 2048, 8192, 1024);
-                    umma_f16_pair(d, da, db, idesc, (kb > kc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < Cfg::BK / 16; ++kk)
+                    umma_f16_pair(d, dA0 + so + (kk * 32 >> 4), dB0 + so + (kk * 2048 >> 4), idesc, 1u);
                 issued = true;
                 umma_commit_pair(smem_u32(&ctl->empty[stage]), BOTH);
                 if (++stage == Cfg::STAGES) {
@@ -792,6 +795,11 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                            Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
     constexpr uint32_t idesc = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
+    // Stage s, k-step kk of the ring differ from stage 0, k-step 0 only in
+    // the start-address field (address >> 4, bits [0,14)); shared memory
+    // stays under 256 KB so the sum never carries out of that field.
+    const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);
+    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, 8192, 1024);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
@@ -818,14 +826,11 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                     ++nkb;
                 }
                 tc_fence_after_sync();
-                const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
-                const uint32_t sb = sa + Cfg::A_BYTES;
+                const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
+                umma_f16(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 16; ++kk) {
-                    const uint64_t da = umma_desc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t db = umma_desc_sw128(sb + kk * 2048, 8192, 1024);
-                    umma_f16(d, da, db, idesc, (kb > kc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < Cfg::BK / 16; ++kk)
+                    umma_f16(d, dA0 + so + (kk * 32 >> 4), dB0 + so + (kk * 2048 >> 4), idesc, 1u);
                 issued = true;
                 umma_commit(smem_u32(&ctl->empty[stage]));
                 if (++stage == Cfg::STAGES) {
