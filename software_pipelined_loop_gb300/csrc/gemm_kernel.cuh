@@ -245,6 +245,8 @@ __device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int64_t unit)
 template <class Cfg>
 struct WorkIter {
     int64_t dp, beg, pos;
+    int64_t t;           // split tile of the next split item (they come last tile first)
+    uint32_t per_group;  // tiles in a group of group_m tile rows
 
     __device__ __forceinline__ explicit WorkIter(const GemmParams &p)
     {
@@ -252,6 +254,8 @@ struct WorkIter {
         dp = u;
         beg = sk_begin(p, u);
         pos = sk_begin(p, u + 1);
+        t = pos > beg ? (pos - 1) / p.num_kb : 0;
+        per_group = static_cast<uint32_t>(p.group_m) * static_cast<uint32_t>(p.tiles / p.m_tiles);
     }
 
     __device__ __forceinline__ bool next(const GemmParams &p, Work &w)
@@ -265,7 +269,6 @@ struct WorkIter {
             w.kind = 0;
             w.sk_tile = -1;
         } else if (pos > beg) {
-            const int64_t t = (pos - 1) / p.num_kb;
             const int64_t ts = t * p.num_kb;
             w.kb1 = pos - ts;
             w.kb0 = beg > ts ? beg - ts : 0;
@@ -273,18 +276,23 @@ struct WorkIter {
             w.kind = w.kb1 < p.num_kb ? 1 : (w.kb0 > 0 ? 2 : 0);
             w.sk_tile = t;
             tile = p.dp_tiles + t;
+            --t;
         } else {
             return false;
         }
         // Grouped order: tile -> (group, index in group); a group holds
         // gm tile rows (the last one may hold fewer) times all columns.
-        const int64_t n_tiles = p.tiles / p.m_tiles;
-        const int64_t per_group = p.group_m * n_tiles;
-        const int64_t g = tile / per_group, in = tile - g * per_group;
-        const int64_t first = g * p.group_m;
-        const int64_t gm = p.m_tiles - first < p.group_m ? p.m_tiles - first : p.group_m;
-        w.m0 = (first + in % gm) * Cfg::TILE_M;
-        w.n0 = (in / gm) * Cfg::BN;
+        // Tile indices fit 32 bits (2^31 tiles of C would not fit in device
+        // memory), and 32-bit division is several times cheaper than 64-bit
+        // on the producer's and epilogue's path.
+        const uint32_t tl = static_cast<uint32_t>(tile);
+        const uint32_t gmax = static_cast<uint32_t>(p.group_m), mt = static_cast<uint32_t>(p.m_tiles);
+        const uint32_t g = tl / per_group, in = tl - g * per_group;
+        const uint32_t first = g * gmax;
+        const uint32_t gm = mt - first < gmax ? mt - first : gmax;
+        const uint32_t col = in / gm;
+        w.m0 = static_cast<int64_t>(first + (in - col * gm)) * Cfg::TILE_M;
+        w.n0 = static_cast<int64_t>(col) * Cfg::BN;
         return true;
     }
 };

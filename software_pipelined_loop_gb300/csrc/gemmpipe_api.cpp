@@ -263,6 +263,9 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     const int64_t tile_m = v->info.pair ? 2 * kBM : kBM;
     pl->m_tiles = (M + tile_m - 1) / tile_m;
     pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
+    // The kernel maps tile indices in 32 bits; a C of 2^31 tiles (at least
+    // 2^38 bytes) cannot be device memory, so such sizes are invalid.
+    if (pl->tiles > INT32_MAX) return GEMMPIPE_ERR_INVALID_VALUE;
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
     // Persistent grid: at most one CTA (or CTA pair) per SM (pair) slot.

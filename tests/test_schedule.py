@@ -123,6 +123,31 @@ def test_schedule_properties(tiles, slots, num_kb, mode):
         assert t >= dp_tiles
 
 
+def items_incremental(u: int, units: int, dp_tiles: int, sk_tiles: int, num_kb: int):
+    """The kernel's form of the same walk: one division per unit for the
+    first split tile, then one tile back per item."""
+    out = [(t, 0, num_kb, 0) for t in range(u, dp_tiles, units)]
+    sk_work = sk_tiles * num_kb
+    beg, pos = sk_begin(sk_work, units, u), sk_begin(sk_work, units, u + 1)
+    t = (pos - 1) // num_kb if pos > beg else 0
+    while pos > beg:
+        ts = t * num_kb
+        kb1 = pos - ts
+        kb0 = beg - ts if beg > ts else 0
+        pos = ts + kb0
+        out.append((dp_tiles + t, kb0, kb1, 1 if kb1 < num_kb else (2 if kb0 > 0 else 0)))
+        t -= 1
+    return out
+
+
+@pytest.mark.parametrize("mode", ["compute", "forced"])
+def test_incremental_split_walk_matches(mode):
+    for tiles, slots, num_kb in CASES:
+        units, dp_tiles, sk_tiles = plan(tiles, slots, num_kb, False, mode == "forced")
+        for u in range(units):
+            assert items_incremental(u, units, dp_tiles, sk_tiles, num_kb) == items(u, units, dp_tiles, sk_tiles, num_kb)
+
+
 def test_balance_when_tiles_overflow_the_grid():
     # Equal shares: every unit's k-block count is within one tile's worth of
     # the mean (whole tiles) plus one k-block (split ranges).
