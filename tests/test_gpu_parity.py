@@ -195,6 +195,17 @@ def test_host_pointer_rejected(dev):
     assert ei.value.status == gemmpipe.ERR_INVALID_VALUE
 
 
+def test_plan_rejects_tile_counts_beyond_32_bits(dev):
+    # 2^24 x 2^24 is 2^32 tiles of 256 x 256: the kernel maps tile indices in
+    # 32 bits, and such a C (2^50 bytes) cannot be device memory.  Only the
+    # plan is asked for: nothing is launched.
+    for dtype in (0, 1):
+        with pytest.raises(gemmpipe.GemmpipeError) as ei:
+            gemmpipe.gemmpipe_plan(dtype, 1 << 24, 1 << 24, 64)
+        assert ei.value.status == gemmpipe.ERR_INVALID_VALUE
+    assert gemmpipe.gemmpipe_plan(1, 1 << 15, 1 << 15, 64)["tiles"] == (1 << 14)
+
+
 # ----------------------------------------------------------- INT8 exactness
 
 @pytest.mark.parametrize("forced", [-1, 0], ids=["widened_in_workspace", "widened_in_kernel_if_aligned"])
