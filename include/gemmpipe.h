@@ -54,7 +54,8 @@
  *
  * Error behaviour common to the GEMM entry points:
  *   - M, N or K negative, any of them above 2^31 - 1, a matrix of 2^56
- *     elements or more, a null A/B with
+ *     elements or more, a C of 2^31 or more 128 x 128 tiles
+ *     (ceil(M/128) * ceil(N/128) > 2^31 - 1), a null A/B with
  *     M*N*K > 0, a null C with M*N > 0, a pointer not aligned to its element
  *     size, or a pointer the CUDA runtime does not know as device or managed
  *     memory                                   -> GEMMPIPE_ERR_INVALID_VALUE

@@ -89,6 +89,10 @@ gemmpipe_status_t check_shape(int64_t M, int64_t N, int64_t K, const void *A, co
     if ((K > 0 && M > kMaxElems / (K + 8)) || (N > 0 && K > kMaxElems / (N + 8)) ||
         (N > 0 && M > kMaxElems / N))
         return GEMMPIPE_ERR_INVALID_VALUE;
+    // The kernels number C's tiles in 32 bits.  Counted in the smallest
+    // tile (128 x 128), a C of 2^31 tiles holds 2^45 values: no device holds
+    // it, so such sizes are refused before anything is launched.
+    if (((M + 127) / 128) * ((N + 127) / 128) > INT32_MAX) return GEMMPIPE_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return GEMMPIPE_OK;
     if (!C) return GEMMPIPE_ERR_INVALID_VALUE;
     if (K > 0 && (!A || !B)) return GEMMPIPE_ERR_INVALID_VALUE;
@@ -263,8 +267,7 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     const int64_t tile_m = v->info.pair ? 2 * kBM : kBM;
     pl->m_tiles = (M + tile_m - 1) / tile_m;
     pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
-    // The kernel maps tile indices in 32 bits; a C of 2^31 tiles (at least
-    // 2^38 bytes) cannot be device memory, so such sizes are invalid.
+    // Already refused by the shape check (tile indices are 32-bit).
     if (pl->tiles > INT32_MAX) return GEMMPIPE_ERR_INVALID_VALUE;
     pl->num_kb = (K + kBK - 1) / kBK;
     pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;

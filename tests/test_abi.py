@@ -63,6 +63,9 @@ def test_host_side_argument_checks(lib):
     big = (1 << 31) - 1
     assert s8(big, 8, big, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE    # 2^62 elements of A
     assert f16(big, big, 8, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE   # 2^62 elements of C
+    # 2^32 tiles of 128 x 128 (C of 2^46 values, under the 2^56-element rule)
+    assert f16(1 << 23, 1 << 23, 8, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
+    assert s8(1 << 23, 1 << 23, 8, fake, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
     assert f16(4, 4, 4, None, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE
     assert s8(4, 4, 4, fake, fake, None, None) == gemmpipe.ERR_INVALID_VALUE
     assert f16(4, 4, 4, fake + 1, fake, fake, None) == gemmpipe.ERR_INVALID_VALUE   # fp16 misaligned

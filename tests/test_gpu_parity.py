@@ -196,7 +196,7 @@ def test_host_pointer_rejected(dev):
 
 
 def test_plan_rejects_tile_counts_beyond_32_bits(dev):
-    # 2^24 x 2^24 is 2^32 tiles of 256 x 256: the kernel maps tile indices in
+    # 2^24 x 2^24 is 2^34 tiles of 128 x 128: the kernels number tiles in
     # 32 bits, and such a C (2^50 bytes) cannot be device memory.  Only the
     # plan is asked for: nothing is launched.
     for dtype in (0, 1):
