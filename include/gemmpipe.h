@@ -222,8 +222,9 @@ GEMMPIPE_API gemmpipe_status_t gemm_f16f32_host(int64_t M, int64_t N, int64_t K,
                                                 float *C, gemmpipe_stream_t stream);
 
 /*
- * Rows per panel of the host-buffer calls: about an eighth of M rounded up
- * to a multiple of 256, at least 512 (so M <= 512 is one panel).  Needs no
+ * Rows per panel of the host-buffer calls: a quarter of M rounded up to a
+ * multiple of 256, at least 512 (so M <= 512 is one panel, and there are at
+ * most four).  Needs no
  * GPU.
  */
 GEMMPIPE_API int64_t gemmpipe_host_panel_rows(int64_t M);

@@ -95,14 +95,14 @@ def test_host_side_argument_checks(lib):
 
 def test_host_panel_rows(lib):
     rows = gemmpipe.gemmpipe_host_panel_rows
-    # At least 512 rows; about M / 8 rounded up to 256 beyond that.
-    assert [rows(m) for m in (0, 1, 512, 513, 4096, 4097, 8192, 16384, 100000)] == \
-        [512, 512, 512, 512, 512, 768, 1024, 2048, 12544]
+    # At least 512 rows; M / 4 rounded up to 256 beyond that.
+    assert [rows(m) for m in (0, 1, 512, 513, 2048, 2049, 4096, 4097, 8192, 16384, 100000)] == \
+        [512, 512, 512, 512, 512, 768, 1024, 1280, 2048, 4096, 25088]
     for m in range(1, 20000, 97):
         r = rows(m)
         assert r % 256 == 0 and r >= 512
         panels = -(-m // r)
-        assert panels <= 8 and (panels == 1 or r * (panels - 1) < m)
+        assert panels <= 4 and (panels == 1 or r * (panels - 1) < m)
 
 
 def test_no_gpu_fails_loudly(lib):
