@@ -74,7 +74,7 @@ SHAPES = [
     (512, 256, 128),     # exactly one panel
     (513, 64, 100),      # two panels, the second one row
     (1300, 1000, 777),   # three panels, ragged last one, odd K
-    (2100, 520, 2048),   # five panels
+    (2100, 520, 2048),   # three panels of 768 rows, the last 564
     # B of at least 4 MiB with N a multiple of 32: the first panel is
     # computed in two column halves as B's halves arrive
     (1100, 2048, 2080),  # INT8 and FP16 split
@@ -168,11 +168,12 @@ def test_host_s8_other_int8_paths(dev, producer):
 
 
 def test_host_s8_full_size_sampled(dev):
-    """INT8 4096^3 (eight panels of 512 rows) through host buffers, checked on
-    sampled rows: the first and last rows of every panel and random ones."""
+    """INT8 4096^3 (four panels of 1024 rows, the first in column halves)
+    through host buffers, checked on sampled rows: the first and last rows of
+    every panel and random ones."""
     M = N = K = 4096
     A, B = inputs.workload_operands(2)[5:7]
     got = run_host("s8", A, B, True)
-    rows = sorted({0, 1, 511, 512, 1023, 2047, 2048, 3583, 3584, 4095} |
+    rows = sorted({0, 1, 511, 512, 1023, 1024, 2047, 2048, 3071, 3072, 4095} |
                   set(int(x) for x in np.random.default_rng(5).integers(0, M, 16)))
     assert np.array_equal(got[rows], oracle.gemm_s8s8s32(A, B, rows=rows))
