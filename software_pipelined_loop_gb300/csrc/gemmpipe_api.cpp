@@ -732,30 +732,33 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 // One host-buffer call: B and the row panels of A go to device buffers on
 // the `in` stream, panel p's GEMM runs on the caller's stream once its rows
 // have arrived, and its rows of C go back on the `out` stream while later
-// panels compute.  With `split_cols` > 0 the first panel is computed in two
-// column halves, [0, split_cols) and the rest: B comes in those halves
-// (first panel's rows of A before them), so the first C values start back
-// after half of B instead of all of it.  `prep_b(c0, nc)` enqueues what B's
-// columns [c0, c0 + nc) need once they have arrived; `panel(r0, mp, c0, nc)`
-// enqueues the kernels of C's rows [r0, r0 + mp) x columns [c0, c0 + nc).
-// Everything is enqueued before the first copy back, so a pageable C (whose
-// copies return only when done) still overlaps the remaining panels.
+// panels compute.  With `parts` > 1 the first panel is computed in that many
+// column parts: B comes in those parts (the first panel's rows of A before
+// them), so the first C values start back after a part of B instead of all
+// of it.  `prep_b(c0, nc)` enqueues what B's columns [c0, c0 + nc) need once
+// they have arrived; `panel(r0, mp, c0, nc)` enqueues the kernels of C's rows
+// [r0, r0 + mp) x columns [c0, c0 + nc).  Everything is enqueued before the
+// first copy back, so a pageable C (whose copies return only when done)
+// still overlaps the remaining panels.
 template <class PrepFn, class PanelFn>
 gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64_t K, const void *A, const void *B,
-                            void *C, int ab_bytes, int c_bytes, void *dA, void *dB, void *dC, int64_t split_cols,
+                            void *C, int ab_bytes, int c_bytes, void *dA, void *dB, void *dC, int parts,
                             PrepFn prep_b, PanelFn panel)
 {
     const int64_t rows = gemmpipe_host_panel_rows(M);
     const int64_t P = (M + rows - 1) / rows;
-    const bool split = split_cols > 0 && split_cols < N && K > 0;
+    const int Q = K > 0 && parts > 1 ? parts : 1;  // column parts of the first panel
+    const int64_t w = Q > 1 ? N / Q / 16 * 16 : N;   // whole 16-column groups: bases stay on 16 bytes
+    const auto col0 = [&](int q) { return q * w; };
+    const auto ncol = [&](int q) { return q == Q - 1 ? N - col0(q) : w; };
     HostPipe h;
-    gemmpipe_status_t st = host_pipe(dev, s, static_cast<size_t>(2 * P + 6), &h);
+    gemmpipe_status_t st = host_pipe(dev, s, static_cast<size_t>(2 * Q + 2 * P + 3), &h);
     if (st != GEMMPIPE_OK) return st;
-    // Events: [0] start, [1] B (or its first half) in, [2] B's second half
-    // in, [3, 3+P) A panels in, [3+P] first panel's first half done,
-    // [4+P, 4+2P) panels done, [4+2P] all in, [5+2P] all out.
+    // Events: [0] start; ev_b[q] B's part q in; ev_a[p] A's panel p in;
+    // ev_h[q] the first panel's part q done; ev_c[p] panel p done (p >= 1);
+    // ev_end[0] all in, ev_end[1] all out.
     cudaEvent_t *ev = h.ev.data();
-    cudaEvent_t *ev_a = ev + 3, *ev_c = ev + 4 + P;
+    cudaEvent_t *ev_b = ev + 1, *ev_a = ev_b + Q, *ev_h = ev_a + P, *ev_c = ev_h + Q, *ev_end = ev_c + P;
     const auto ok = [](cudaError_t e) {
         if (e == cudaSuccess) return true;
         cudaGetLastError();
@@ -788,48 +791,33 @@ gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64
     };
     bool good = true;
     if (K > 0) {
-        if (split) {
-            good = copy_a(0) && copy_b(0, split_cols) && ok(cudaEventRecord(ev[1], h.in)) &&
-                   copy_b(split_cols, N - split_cols) && ok(cudaEventRecord(ev[2], h.in));
-            for (int64_t p = 1; good && p < P; ++p) good = copy_a(p);
-        } else {
-            good = copy_b(0, N) && ok(cudaEventRecord(ev[1], h.in));
-            for (int64_t p = 0; good && p < P; ++p) good = copy_a(p);
-        }
+        if (Q > 1) good = copy_a(0);
+        for (int q = 0; good && q < Q; ++q) good = copy_b(col0(q), ncol(q)) && ok(cudaEventRecord(ev_b[q], h.in));
+        for (int64_t p = Q > 1 ? 1 : 0; good && p < P; ++p) good = copy_a(p);
     }
     auto wait = [&](cudaEvent_t e) { return K == 0 || ok(cudaStreamWaitEvent(s, e, 0)); };
-    if (good) {
-        if (split) {
-            good = wait(ev_a[0]) && wait(ev[1]);
-            if (good && (st = prep_b(0, split_cols)) == GEMMPIPE_OK && (st = panel(0, rows_of(0), 0, split_cols)) ==
-                                                                            GEMMPIPE_OK) {
-                good = ok(cudaEventRecord(ev[3 + P], s)) && wait(ev[2]);
-                if (good && (st = prep_b(split_cols, N - split_cols)) == GEMMPIPE_OK &&
-                    (st = panel(0, rows_of(0), split_cols, N - split_cols)) == GEMMPIPE_OK)
-                    good = ok(cudaEventRecord(ev_c[0], s));
-            }
-        } else {
-            good = wait(ev[1]) && wait(ev_a[0]);
-            if (good && (st = prep_b(0, N)) == GEMMPIPE_OK && (st = panel(0, rows_of(0), 0, N)) == GEMMPIPE_OK)
-                good = ok(cudaEventRecord(ev_c[0], s));
-        }
+    if (good) good = wait(ev_a[0]);
+    for (int q = 0; good && st == GEMMPIPE_OK && q < Q; ++q) {
+        good = wait(ev_b[q]);
+        if (good && (st = prep_b(col0(q), ncol(q))) == GEMMPIPE_OK &&
+            (st = panel(0, rows_of(0), col0(q), ncol(q))) == GEMMPIPE_OK)
+            good = ok(cudaEventRecord(ev_h[q], s));
     }
     for (int64_t p = 1; good && st == GEMMPIPE_OK && p < P; ++p) {
         good = wait(ev_a[p]);
         if (good && (st = panel(p * rows, rows_of(p), 0, N)) == GEMMPIPE_OK) good = ok(cudaEventRecord(ev_c[p], s));
     }
     if (good && st == GEMMPIPE_OK) {
-        if (split) {
-            const size_t r = static_cast<size_t>(rows_of(0));
-            good = ok(cudaStreamWaitEvent(h.out, ev[3 + P], 0)) &&
-                   ok(cudaMemcpy2DAsync(hC, crow, dCc, crow, static_cast<size_t>(split_cols * c_bytes), r,
-                                        cudaMemcpyDefault, h.out)) &&
-                   ok(cudaStreamWaitEvent(h.out, ev_c[0], 0)) &&
-                   ok(cudaMemcpy2DAsync(hC + split_cols * c_bytes, crow, dCc + split_cols * c_bytes, crow,
-                                        static_cast<size_t>((N - split_cols) * c_bytes), r, cudaMemcpyDefault,
-                                        h.out));
+        const size_t r = static_cast<size_t>(rows_of(0));
+        for (int q = 0; good && q < Q; ++q) {
+            good = ok(cudaStreamWaitEvent(h.out, ev_h[q], 0));
+            if (good && Q == 1)
+                good = ok(cudaMemcpyAsync(hC, dCc, r * crow, cudaMemcpyDefault, h.out));
+            else if (good)
+                good = ok(cudaMemcpy2DAsync(hC + col0(q) * c_bytes, crow, dCc + col0(q) * c_bytes, crow,
+                                            static_cast<size_t>(ncol(q) * c_bytes), r, cudaMemcpyDefault, h.out));
         }
-        for (int64_t p = split ? 1 : 0; good && p < P; ++p) {
+        for (int64_t p = 1; good && p < P; ++p) {
             const int64_t r0 = p * rows;
             good = ok(cudaStreamWaitEvent(h.out, ev_c[p], 0)) &&
                    ok(cudaMemcpyAsync(hC + r0 * crow, dCc + r0 * crow, static_cast<size_t>(rows_of(p)) * crow,
@@ -838,18 +826,23 @@ gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64
     }
     // Whatever was enqueued, the caller's stream ends after both side
     // streams, so later work on it never races these copies.
-    const bool joined = ok(cudaEventRecord(ev[4 + 2 * P], h.in)) && ok(cudaEventRecord(ev[5 + 2 * P], h.out)) &&
-                        ok(cudaStreamWaitEvent(s, ev[4 + 2 * P], 0)) && ok(cudaStreamWaitEvent(s, ev[5 + 2 * P], 0));
+    const bool joined = ok(cudaEventRecord(ev_end[0], h.in)) && ok(cudaEventRecord(ev_end[1], h.out)) &&
+                        ok(cudaStreamWaitEvent(s, ev_end[0], 0)) && ok(cudaStreamWaitEvent(s, ev_end[1], 0));
     if (st != GEMMPIPE_OK) return st;
     return good && joined ? GEMMPIPE_OK : GEMMPIPE_ERR_LAUNCH;
 }
 
-// Columns of the first panel's first half when splitting pays: B of at least
-// 4 MiB, and halves that keep every TMA base and pitch on 16 bytes.
-int64_t host_split_cols(int64_t N, int64_t K, int ab_bytes)
+// Column parts of the first panel: two (halves) when B holds at least 4 MiB
+// and N is a multiple of 32, else one; parts are whole 16-column groups, so
+// every TMA base and pitch stays on 16 bytes.  End to end at 4096^3 (four
+// panels), INT8 / FP16: 523 / 628 us in one part, 491 / 592 us in halves,
+// 500 / 615 us in quarters -- more, smaller copies cost more than the
+// earlier start saves.
+int host_col_parts(int64_t N, int64_t K, int ab_bytes)
 {
-    if (N % 32 != 0 || N < 512 || K * N * ab_bytes < (int64_t(4) << 20)) return 0;
-    return N / 2 / 16 * 16;
+    const int64_t b = K * N * ab_bytes;
+    if (N % 32 == 0 && N >= 512 && b >= (int64_t(4) << 20)) return 2;
+    return 1;
 }
 
 // Device buffers of a host-buffer call: A, B and C, each 256-byte aligned.
@@ -921,8 +914,8 @@ gemmpipe_status_t gemm_s8s8s32_host(int64_t M, int64_t N, int64_t K, const int8_
         tr.end();
         return launched(e);
     };
-    const int64_t split = direct ? 0 : host_split_cols(N, K, 1);
-    return host_call(dev, s, M, N, K, A, B, C, 1, 4, dA, dB, dC, split, prep_b,
+    const int parts = direct ? 1 : host_col_parts(N, K, 1);
+    return host_call(dev, s, M, N, K, A, B, C, 1, 4, dA, dB, dC, parts, prep_b,
                      [&](int64_t r0, int64_t mp, int64_t c0, int64_t nc) {
         if (direct) return gemm_s8s8s32(mp, N, K, A8 + r0 * K, B8, C32 + r0 * N, stream);
         gemmpipe_status_t e;
@@ -955,10 +948,10 @@ gemmpipe_status_t gemm_f16f32_host(int64_t M, int64_t N, int64_t K, const gemmpi
     const gemmpipe_half_t *A16 = static_cast<const gemmpipe_half_t *>(dA);
     const gemmpipe_half_t *B16 = static_cast<const gemmpipe_half_t *>(dB);
     float *C32 = static_cast<float *>(dC);
-    // The first panel's column halves run as plans on B's column slices,
+    // The first panel's column parts run as plans on B's column slices,
     // which needs TMA-describable operands (K a multiple of 8).
-    const int64_t split = K % 8 == 0 ? host_split_cols(N, K, 2) : 0;
-    return host_call(dev, s, M, N, K, A, B, C, 2, 4, dA, dB, dC, split,
+    const int parts = K % 8 == 0 ? host_col_parts(N, K, 2) : 1;
+    return host_call(dev, s, M, N, K, A, B, C, 2, 4, dA, dB, dC, parts,
                      [](int64_t, int64_t) { return GEMMPIPE_OK; },
                      [&](int64_t r0, int64_t mp, int64_t c0, int64_t nc) {
         if (nc == N) return gemm_f16f32(mp, N, K, A16 + r0 * K, B16, C32 + r0 * N, stream);

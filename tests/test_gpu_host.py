@@ -76,10 +76,11 @@ SHAPES = [
     (1300, 1000, 777),   # three panels, ragged last one, odd K
     (2100, 520, 2048),   # three panels of 768 rows, the last 564
     # B of at least 4 MiB with N a multiple of 32: the first panel is
-    # computed in two column halves as B's halves arrive
+    # computed in column parts as B's parts arrive
     (1100, 2048, 2080),  # INT8 and FP16 split
     (600, 4096, 1024),   # one panel, split
     (700, 2048, 2051),   # INT8 split (any K); FP16 not (K not a multiple of 8)
+    (700, 1024, 16384),  # long K (16 MiB of int8 B), first panel in halves
 ]
 
 
