@@ -10,11 +10,33 @@ another 256 MiB read between timed steps (no input cached, no dirty lines
 left for the timed step to write back), and each step is timed alone with
 CUDA events on its stream.
 
-Also measured in the same run and reported under ``secondary``: FP16
-4096^3 (TFLOPS), the skinny FP16 16384 x 128 x 16384 (GB/s of algorithmic
-bytes: A, B and C moved once), the ragged FP16 4093 x 3001 x 4107, and the
-two small cases INT8 512^3 and FP16 1024^3 (launch- and latency-bound:
-reported, not targets).
+``roofline`` is the GEMM kernel alone: 2 M N K over the mean of the CUDA
+events the library records around that kernel on its launch stream, in a
+second pass of the same timed steps (those events stop the GEMM's
+programmatic early launch, so the first pass, which gives ``value``, runs
+without them).  ``peak`` is the measured bf16 burst figure (the fp16
+tcgen05 pipe runs at the bf16 rate; INT8 runs on that pipe too), or HBM
+copy bandwidth for the skinny shape.  ``traffic`` is the DRAM bytes of one
+ncu capture of the same kernel sources (null once they change).
+
+``parity``: every timed output (the C of the last timed step) is compared
+with the CPU oracle's whole product -- bit for bit for INT8, max-abs 1e-2 and
+relative Frobenius 1e-4 for FP16 -- and the oracle's wall time on all host
+cores is each workload's CPU baseline (``cpu_baseline`` for the headline,
+``cpu`` in each secondary entry).
+
+``e2e`` is the same headline through the host-buffer call
+gemm_s8s8s32_host: page-locked A and B in, C out, inside the timed region.
+``int8_step_floor`` puts the step beside its floor (the widening pass at the
+in-run copy rate plus the GEMM kernel); ``library_context`` times cuBLAS FP16
+and torch._int_mm on the same shape and the pages' own design (warp-level
+integer MMA, the legacy INT8 ceiling) -- context, not the hot path.
+
+``secondary`` (last in the line): INT8 512^3 and FP16 1024^3 (launch- and
+latency-bound, reported only), the ragged FP16 4093 x 3001 x 4107, the skinny
+FP16 16384 x 128 x 16384 (GB/s of algorithmic bytes: A, B and C moved once)
+and FP16 4096^3 (TFLOPS), each with its step time, kernel time, fractions of
+peak per kernel (``frac``) and per step (``step_frac``), parity and CPU time.
 
 ``--impl reference`` times the CPU oracle on the host cores instead, on a
 bounded sample of rows of the same workload.
@@ -45,15 +67,15 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM bytes (read + write) per launch of a kernel variant, from one
-# `ncu --set full` capture (profiles/), valid only while the kernel sources
-# hash as they did when the counters were taken.
+# `ncu --set full` capture of that launch, valid only while the kernel
+# sources hash as they did when the counters were taken (else null).
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu"]
 TRAFFIC = {
-    # (dtype, M, N, K, cta pair, BN): (bytes per launch, sources hash, profile)
-    ("s8", 4096, 4096, 4096, 1, 256): (139_024_640, "b8ac23c89f1e0055", "profiles/gemm_pair_int8_4096.md"),
-    ("f16", 4096, 4096, 4096, 1, 256): (139_781_120, "b8ac23c89f1e0055", "profiles/gemm_pair_f16_4096.md"),
-    ("f16", 16384, 128, 16384, 0, 128): (544_346_880, "b8ac23c89f1e0055", "profiles/gemm_skinny_f16_16384x128x16384.md"),
-    ("f16", 4093, 3001, 4107, 1, 256): (112_088_064, "b8ac23c89f1e0055", "profiles/gemm_pair_f16_ragged_4093x3001x4107.md"),
+    # (dtype, M, N, K, cta pair, BN): (bytes per launch, sources hash)
+    ("s8", 4096, 4096, 4096, 1, 256): (139_024_640, "b8ac23c89f1e0055"),
+    ("f16", 4096, 4096, 4096, 1, 256): (139_781_120, "b8ac23c89f1e0055"),
+    ("f16", 16384, 128, 16384, 0, 128): (544_346_880, "b8ac23c89f1e0055"),
+    ("f16", 4093, 3001, 4107, 1, 256): (112_088_064, "b8ac23c89f1e0055"),
 }
 
 
@@ -66,12 +88,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(dtype: str, plan: dict, shape: tuple) -> tuple[int | None, str | None]:
+def measured_traffic(dtype: str, plan: dict, shape: tuple) -> int | None:
     """Captured DRAM traffic of the launch this plan runs on this shape, or None."""
     t = TRAFFIC.get((dtype, *shape, plan["cta_pair"], plan["BN"]))
     if t is None or t[1] != kernel_source_hash():
-        return None, None
-    return t[0], t[2]
+        return None
+    return t[0]
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -196,7 +218,7 @@ def run_reference(args) -> int:
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
-        "config": {"workload": name, "M": M, "N": N, "K": K},
+        "config": bench_config(name, M, N, K, "flushed" if A.nbytes + B.nbytes < FLUSH_BYTES else "inputs > L2"),
         "cpu_baseline": {"value": v, "unit": "TOPS", "cores": cores, "kind": "oracle",
                          "sample": f"first {rows} of {M} rows of C per step (all {N} columns, full K)"},
         "e2e": {"value": v, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -206,10 +228,6 @@ def run_reference(args) -> int:
 
 
 # ------------------------------------------------------------------ GPU arm
-
-KERNEL_TIMING = ("GEMM kernel: mean of the library's CUDA events around each launch, on the launch stream, "
-                 "over a second pass of the same timed steps")
-
 
 def time_steps(call, steps: int, flush=None, stream=None) -> list[float]:
     """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each."""
@@ -272,25 +290,17 @@ def measure_gemm(wl, steps: int, warmup: int, dev, flush, peaks, peak_src):
     kernel_ms = gemm_ms / max(1, gemm_n)
     plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K, Ad, Bd, C)
     skinny = N <= 128
+    traffic = measured_traffic(dtype, plan, (M, N, K))
     if skinny:
         peak = peaks["hbm_gbs"]
         achieved = alg_bytes / kernel_ms / 1e6
-        traffic, prof = measured_traffic(dtype, plan, (M, N, K))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_source": f"hbm_gbs ({peak_src})"}
-        if prof:
-            roof["traffic_source"] = prof
-        roof["kernel_timing"] = KERNEL_TIMING
+                "traffic": traffic, "peak_source": f"hbm_gbs, {peak_src}"}
     else:
         peak = peaks["bf16_tflops"]
         achieved = flops / kernel_ms / 1e9
-        traffic, prof = measured_traffic(dtype, plan, (M, N, K))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"bf16_tflops burst ({peak_src}); kind::f16 runs at the bf16 rate"}
-        if prof:
-            roof["traffic_source"] = prof
-        roof["kernel_timing"] = KERNEL_TIMING
+                "frac": achieved / peak, "traffic": traffic, "peak_source": f"bf16_tflops burst, {peak_src}"}
     return {
         "name": name, "dtype": dtype, "M": M, "N": N, "K": K, "ms": ms, "ms_median": statistics.median(times),
         "ops_per_s": flops / ms / 1e9, "bytes_per_s": alg_bytes / ms / 1e6, "kernel_ms": kernel_ms,
@@ -359,6 +369,103 @@ def measure_copy_ref(dev, peaks: dict, reps: int = 10) -> dict:
             "gbs": gbs, "of_measured_hbm_peak": gbs / peaks["hbm_gbs"]}
 
 
+def parity_check(res: dict) -> dict:
+    """The timed call's C (the output of its last timed step) against the
+    CPU oracle's whole product, every element: bit-exact for INT8, max-abs
+    <= 1e-2 and relative Frobenius <= 1e-4 for FP16.  The oracle's wall time
+    on the host cores is this workload's CPU baseline."""
+    import numpy as np
+
+    import oracle
+    A, B = res["A"], res["B"]
+    threads = oracle.default_threads()
+    t = time.perf_counter()
+    want = oracle.gemm_s8s8s32(A, B, threads=threads) if res["dtype"] == "s8" else \
+        oracle.gemm_f16f32(A, B, threads=threads)
+    secs = time.perf_counter() - t
+    got = res["C"].cpu().numpy()
+    if res["dtype"] == "s8":
+        bad = int(np.count_nonzero(got != want))
+        ok = bad == 0
+        verdict = f"bit-exact, all {got.size} elements" if ok else f"FAIL: {bad} of {got.size} elements differ"
+    else:
+        d = got.astype(np.float64) - want.astype(np.float64)
+        err = float(np.abs(d).max()) if d.size else 0.0
+        nrm = float(np.linalg.norm(want.astype(np.float64)))
+        rel = float(np.linalg.norm(d) / nrm) if nrm > 0 else float(np.linalg.norm(d))
+        ok = bool(np.isfinite(got).all()) and err <= 1e-2 and rel <= 1e-4
+        verdict = f"{'ok' if ok else 'FAIL'}: all {got.size} elements, max-abs {err:.2e}, rel-fro {rel:.2e}"
+    return {"ok": ok, "verdict": verdict, "oracle_s": secs, "cores": threads,
+            "oracle_rate": res["flops"] / secs / 1e12}
+
+
+def library_context(dev, flush, steps: int) -> dict:
+    """Library calls on the 4096^3 operands, timed like the steps above
+    (L2 flushed, CUDA events): cuBLAS FP16 through torch (fp32 output where
+    this torch offers it) and torch._int_mm INT8.  Context only; nothing of
+    libgemmpipe runs here."""
+    import torch
+
+    from software_pipelined_loop_gb300 import inputs
+    out = {}
+    M = N = K = 4096
+    A, B = inputs.make_operands("f16", M, N, K, inputs.SEED_BASE + 5)
+    Ad, Bd = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        torch.mm(Ad[:8, :8], Bd[:8, :8], out_dtype=torch.float32)
+        call, label = (lambda: torch.mm(Ad, Bd, out_dtype=torch.float32)), "cublas_f16_f32out_4096"
+    except (TypeError, RuntimeError):
+        call, label = (lambda: torch.mm(Ad, Bd)), "cublas_f16_f16out_4096"
+    for _ in range(3):
+        call()
+    ms = statistics.mean(time_steps(call, steps, flush, stream))
+    out[label] = {"ms": ms, "tflops": 2.0 * M * N * K / ms / 1e9}
+    A8, B8 = inputs.make_operands("s8", M, N, K, inputs.SEED_BASE + 2)
+    A8d, B8d = torch.from_numpy(A8).to(dev), torch.from_numpy(B8).to(dev)
+    try:
+        call = lambda: torch._int_mm(A8d, B8d)
+        for _ in range(3):
+            call()
+        ms = statistics.mean(time_steps(call, steps, flush, stream))
+        out["torch_int_mm_s8_4096"] = {"ms": ms, "tops": 2.0 * M * N * K / ms / 1e9}
+    except RuntimeError as e:
+        out["torch_int_mm_s8_4096"] = {"unavailable": str(e).splitlines()[0][:120]}
+    return out
+
+
+def legacy_int8_ceiling(head: dict, dev, flush, steps: int) -> dict:
+    """INT8 4096^3 on the library's comparison path: the pages' own design
+    (warp-level mma.sync m16n8k32 s8 -> s32 fed by a cp.async ring),
+    recompiled for sm_103a.  Its GEMM-kernel rate is the legacy integer-MMA
+    ceiling, the second denominator of the INT8 fraction."""
+    import torch
+
+    from software_pipelined_loop_gb300 import gemmpipe
+    M, N, K = head["M"], head["N"], head["K"]
+    Ad, Bd = torch.from_numpy(head["A"]).to(dev), torch.from_numpy(head["B"]).to(dev)
+    C = torch.empty((M, N), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    gemmpipe.gemmpipe_set_plan_override(2, 0, 0, -1, -1)
+    try:
+        call = lambda: gemmpipe.gemm_s8s8s32(M, N, K, Ad, Bd, C, stream)
+        call()
+        torch.cuda.synchronize()
+        gemmpipe.gemmpipe_timing_read()
+        gemmpipe.gemmpipe_timing_enable(True)
+        time_steps(call, steps, flush, stream)
+        gms, gn, _, _ = gemmpipe.gemmpipe_timing_read()
+        gemmpipe.gemmpipe_timing_enable(False)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    if gemmpipe.gemmpipe_get_device_status(stream) != gemmpipe.OK:
+        raise RuntimeError("legacy INT8 path: device status not OK")
+    if not torch.equal(C, head["C"]):
+        raise RuntimeError("legacy INT8 path: C differs from the tcgen05 path's C")
+    kms = gms / max(1, gn)
+    return {"kernel_ms": kms, "tops": head["flops"] / kms / 1e9}
+
+
 def slowest_rank_ms(ms: float, dist=None, device=None) -> float:
     """Max over ranks of a per-step time (the job's step time)."""
     if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
@@ -420,13 +527,19 @@ def run_gpu(args) -> int:
         clocks = clock.summary(*head["window"])
         if clocks["samples"] < 3:
             clocks["window"] = "whole GPU phase (timed region shorter than the sampling period)"
-        secondary = {}
+        secondary = []
         if not args.no_secondary:
-            for wl in (fp16_4096(), workload(3), workload(4), workload(0), workload(1)):
-                r = measure_gemm(wl, max(10, args.steps // 4), args.warmup, dev, flush, peaks, peak_src)
-                secondary[r["name"]] = r
+            # Small cases first, the metric's FP16 4096^3 and skinny last.
+            for wl in (workload(0), workload(1), workload(4), workload(3), fp16_4096()):
+                secondary.append(measure_gemm(wl, max(10, args.steps // 4), args.warmup, dev, flush, peaks,
+                                              peak_src))
         e2e = measure_e2e(head, max(5, args.steps // 4), dev)
         copy_ref = measure_copy_ref(dev, peaks)
+        context = None
+        if not args.no_secondary and world == 1:
+            context = library_context(dev, flush, max(10, args.steps // 4))
+            if head["dtype"] == "s8":
+                context["int8_legacy_ceiling"] = legacy_int8_ceiling(head, dev, flush, 5)
     finally:
         clock.stop()
 
@@ -439,52 +552,79 @@ def run_gpu(args) -> int:
             dist.destroy_process_group()
         return 0
 
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        r = cpu_oracle_rate(head["A"], head["B"], head["dtype"], target_s=args.cpu_seconds)
-        cpu = {"value": r["value"], "unit": unit, "cores": r["cores"], "kind": "oracle",
-               "sample": f"first {r['rows']} of {head['M']} rows of C (all {head['N']} columns, full K), "
-                         f"{r['seconds']:.1f} s"}
+    # Every timed output against the oracle's whole product (rank 0 at N = 1;
+    # the replicas of other ranks compute the same C).
+    parity, cpu = {}, None
+    if world == 1 and not args.no_parity:
+        for r in [head] + secondary:
+            r["parity"] = parity_check(r)
+            parity[r["name"]] = r["parity"]["verdict"]
+        pc = head["parity"]
+        cpu = {"value": pc["oracle_rate"], "unit": unit, "cores": pc["cores"], "kind": "oracle",
+               "sample": f"the whole workload: all {head['M']} x {head['N']} elements of C, full K, "
+                         f"{pc['oracle_s']:.1f} s",
+               "parity": pc["verdict"]}
+
+    int8_floor = None
+    if head["dtype"] == "s8":
+        # The step is the widening pass plus the GEMM kernel: with the pass
+        # at the in-run copy rate, the step cannot beat this floor unless
+        # the GEMM kernel itself gets faster.
+        widen_bytes = 3 * (head["A"].nbytes + head["B"].nbytes)
+        widen_ms = widen_bytes / copy_ref["gbs"] / 1e6
+        int8_floor = {"widen_ms": head["aux_ms"], "widen_at_copy_rate_ms": widen_ms,
+                      "kernel_ms": head["kernel_ms"], "floor_ms": widen_ms + head["kernel_ms"],
+                      "step_ms": head["ms"], "step_frac": head["flops"] / head["ms"] / 1e9 / peaks["bf16_tflops"],
+                      "kernel_frac": head["roofline"]["frac"]}
+        if context and "int8_legacy_ceiling" in context:
+            lc = context["int8_legacy_ceiling"]
+            int8_floor["step_vs_legacy_ceiling"] = (head["flops"] / head["ms"] / 1e9) / lc["tops"]
 
     def brief(r):
-        unit = "GB/s" if r["N"] <= 128 else ("TOPS" if r["dtype"] == "s8" else "TFLOPS")
-        val = r["bytes_per_s"] if r["N"] <= 128 else r["ops_per_s"]
-        return {"value": val, "unit": unit, "ms_per_step": r["ms"], "kernel_ms": r["kernel_ms"],
-                "roofline": r["roofline"], "l2": r["l2"],
-                "plan": {k: r["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair",
-                                                   "grid", "units", "tiles", "split_tiles", "k_blocks",
-                                                   "smem_bytes", "operand_copy")},
-                "shape": [r["M"], r["N"], r["K"]], "dtype": r["dtype"]}
+        skinny = r["N"] <= 128
+        unit = "GB/s" if skinny else ("TOPS" if r["dtype"] == "s8" else "TFLOPS")
+        val = r["bytes_per_s"] if skinny else r["ops_per_s"]
+        peak = r["roofline"]["peak"]
+        out = {"value": round(val, 1), "unit": unit, "ms": round(r["ms"], 5), "kernel_ms": round(r["kernel_ms"], 5),
+               "frac": round(r["roofline"]["frac"], 3), "step_frac": round(val / peak, 3),
+               "traffic": r["roofline"]["traffic"]}
+        if "parity" in r:
+            out["parity"] = r["parity"]["verdict"]
+            out["cpu"] = {"value": round(r["parity"]["oracle_rate"], 4), "unit": "TOPS" if r["dtype"] == "s8"
+                          else "TFLOPS", "s": round(r["parity"]["oracle_s"], 2), "cores": r["parity"]["cores"]}
+        return out
 
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_median,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": head["dtype"],
-        "dtype_note": ("int8 operands widened to fp16 (exact), tcgen05 kind::f16 with fp32 accumulation "
-                       "in <=1024-k chunks, exact int32 sum") if head["dtype"] == "s8" else
-                      "fp16 operands, tcgen05 kind::f16, fp32 accumulation and output",
         "data": "synthetic",
-        "config": {"workload": head["name"], "M": head["M"], "N": head["N"], "K": head["K"],
-                   "l2": head["l2"] + " (between timed steps: 256 MiB written, then another 256 MiB read, "
-                                      "when inputs < L2)",
-                   "plan": {k: head["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair",
-                                                         "grid", "units", "tiles", "split_tiles", "k_blocks",
-                                                         "smem_bytes", "operand_copy")},
-                   "replicas": world},
+        "config": bench_config(head["name"], head["M"], head["N"], head["K"], head["l2"]),
         "roofline": head["roofline"],
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "copy_ref": copy_ref,
         "gpu_launches": head["launches"],
         "clocks": clocks,
+        "parity": parity or None,
         "kernel_ms": head["kernel_ms"], "aux_ms": head["aux_ms"],
-        "secondary": {k: brief(v) for k, v in secondary.items()},
+        "plan": {k: head["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair", "grid",
+                                              "units", "tiles", "split_tiles", "k_blocks", "operand_copy")},
+        "copy_ref_gbs": round(copy_ref["gbs"], 1),
+        "int8_step_floor": int8_floor,
+        "library_context": context,
+        "secondary": {r["name"]: brief(r) for r in secondary},
     }
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def bench_config(name: str, M: int, N: int, K: int, l2: str) -> dict:
+    """The `config` object of both arms' lines (the same workload)."""
+    return {"workload": name, "M": M, "N": N, "K": K,
+            "l2": l2 + " (between timed steps: 256 MiB written, then another 256 MiB read, when inputs < L2)"}
 
 
 def fp16_4096():
@@ -590,8 +730,8 @@ def main() -> int:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-parity", "--no-cpu-baseline", dest="no_parity", action="store_true",
+                    help="skip the whole-C oracle comparison (and with it the CPU baselines)")
     ap.add_argument("--ref-seconds", type=float, default=None,
                     help="CPU seconds per reference step (default: 4, or 120 / steps when that is less)")
     ap.add_argument("--shape", default=None,

@@ -152,8 +152,13 @@ GEMMPIPE_API gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K,
  *
  * How: the fp16 copies of A and B live in one fixed scratch array of
  * GEMMPIPE_NOALLOC_SCRATCH_BYTES that the library declares statically in
- * device memory.  Every GPU on which the library is loaded holds that array
- * until the process exits.  The caller still passes A, B and C.
+ * device memory.  The CUDA runtime creates that array on a device when it
+ * loads the library's device code there -- with lazy module loading (the
+ * default), during the first call of this entry point on that device -- and
+ * the device holds it until the process exits.  So make one call per device
+ * at start-up, while memory is still free; a device without room for the
+ * array gives GEMMPIPE_ERR_OUT_OF_MEMORY on that call.  The caller still
+ * passes A, B and C.
  *
  * Limits and behaviour:
  *   - needs 2 * (M * Kp + K * Np) <= GEMMPIPE_NOALLOC_SCRATCH_BYTES, with
@@ -162,7 +167,9 @@ GEMMPIPE_API gemmpipe_status_t gemm_f16f32(int64_t M, int64_t N, int64_t K,
  *     GEMMPIPE_ERR_INVALID_VALUE before anything is launched;
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current, and keeps it; make
- *     that first call before any stream capture;
+ *     that first call before any stream capture, and do not reset the
+ *     device (cudaDeviceReset) while the library is in use, since the kept
+ *     address would then be stale;
  *   - all calls share the one array and it keeps whatever the last call
  *     left there; nothing in it has to start at zero, because each call
  *     writes every scratch element it later reads;
@@ -202,8 +209,12 @@ GEMMPIPE_API gemmpipe_status_t gemm_s8s8s32_noalloc(int64_t M, int64_t N, int64_
  * `stream` before reading C.  With pageable memory the CUDA runtime makes
  * the copies synchronous, so the call returns when C has been written (the
  * copies back still overlap the later panels' GEMMs).  The caller keeps A,
- * B and C allocated and A, B unchanged until then.  Calls on one stream
- * from several host threads must be ordered by the caller.
+ * B and C allocated and A, B unchanged until then.  Host-buffer calls on
+ * one stream must be issued from one host thread, or under the caller's own
+ * lock: the side streams and events kept for that stream are shared, and two
+ * calls enqueued at the same time can interleave their event records, so
+ * that a copy back waits on the other call's event and reads C rows before
+ * they are written.
  *
  * Memory: device buffers for A, B and C (M*K + K*N + M*N*4 bytes for INT8,
  * 2*M*K + 2*K*N + 4*M*N for FP16) in a per-(device, stream) workspace, plus
@@ -362,11 +373,13 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int t
  * FP16 CTA-pair kernel with a 6- or 1-stage ring (the two kernels compiled
  * with the trace; any other launch consumes the hook and records nothing),
  * CTA 0 (the leader CTA of pair 0) writes %globaltimer nanoseconds into `buffer`, a
- * device array of 2 * `entries` uint64: element j (j < entries) when its
+ * device array of 3 * `entries` uint64: element j (j < entries) when its
  * producer has issued the tile copies of its j-th k-block (counted over the
  * CTA's whole schedule), element entries + j when its MMA thread finds that
- * k-block's data ready, just before issuing its MMAs.  Elements past the
- * CTA's k-blocks are left as they were.  entries = 0 clears the hook;
+ * k-block's data ready, just before issuing its MMAs, and element
+ * 2 * entries + j the SM's %clock64 cycle count at that same moment (so
+ * time per k-block can be split into cycles and clock rate).  Elements past
+ * the CTA's k-blocks are left as they were.  entries = 0 clears the hook;
  * entries above 2^20, or a buffer that is not device memory, give
  * INVALID_VALUE.
  */

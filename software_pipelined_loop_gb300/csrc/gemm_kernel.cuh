@@ -760,7 +760,10 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                     break;
                 }
                 if constexpr (Cfg::TRACE) {
-                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) p.trace[p.trace_n + nkb] = globaltimer_ns();
+                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
+                        p.trace[p.trace_n + nkb] = globaltimer_ns();
+                        p.trace[2 * p.trace_n + nkb] = sm_clock64();
+                    }
                     ++nkb;
                 }
                 tc_fence_after_sync();
@@ -830,7 +833,10 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                     break;
                 }
                 if constexpr (Cfg::TRACE) {
-                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) p.trace[p.trace_n + nkb] = globaltimer_ns();
+                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
+                        p.trace[p.trace_n + nkb] = globaltimer_ns();
+                        p.trace[2 * p.trace_n + nkb] = sm_clock64();
+                    }
                     ++nkb;
                 }
                 tc_fence_after_sync();

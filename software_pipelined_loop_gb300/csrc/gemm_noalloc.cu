@@ -24,7 +24,10 @@ static __device__ __align__(256) uint16_t g_s8_scratch[kScratchBytes / 2];
 std::atomic<uint16_t *> g_scratch_addr[128];
 
 // Device address of g_s8_scratch on the current device (looked up on the
-// first call made with that device current).
+// first call made with that device current).  Under CUDA's lazy module
+// loading that lookup is also what loads this file's device code on the
+// device and so creates the array; a device without room for it gives
+// GEMMPIPE_ERR_OUT_OF_MEMORY.
 gemmpipe_status_t scratch_address(uint16_t **out)
 {
     int dev = -1;
@@ -35,9 +38,10 @@ gemmpipe_status_t scratch_address(uint16_t **out)
     uint16_t *p = g_scratch_addr[dev].load();
     if (!p) {
         void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_s8_scratch) != cudaSuccess || !a) {
+        const cudaError_t e = cudaGetSymbolAddress(&a, g_s8_scratch);
+        if (e != cudaSuccess || !a) {
             cudaGetLastError();
-            return GEMMPIPE_ERR_LAUNCH;
+            return e == cudaErrorMemoryAllocation ? GEMMPIPE_ERR_OUT_OF_MEMORY : GEMMPIPE_ERR_LAUNCH;
         }
         p = static_cast<uint16_t *>(a);
         g_scratch_addr[dev].store(p);

@@ -40,7 +40,8 @@ struct GemmParams {
     // Test hook: CTA 0 (the leader of pair 0) stamps %globaltimer into
     // trace[j] when its producer has issued the copies of its j-th k-block
     // and into trace[trace_n + j] when its MMA thread finds that k-block's
-    // data ready, for j < trace_n (nullptr: off).
+    // data ready, with the SM's %clock64 at that moment in
+    // trace[2 * trace_n + j], for j < trace_n (nullptr: off).
     unsigned long long *trace = nullptr;
     int64_t trace_n = 0;
     uint64_t timeout_ns;   // bound of every pipeline wait

@@ -732,9 +732,9 @@ int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 // One host-buffer call: B and the row panels of A go to device buffers on
 // the `in` stream, panel p's GEMM runs on the caller's stream once its rows
 // have arrived, and its rows of C go back on the `out` stream while later
-// panels compute.  With `parts` > 1 the first panel is computed in that many
-// column parts: B comes in those parts (the first panel's rows of A before
-// them), so the first C values start back after a part of B instead of all
+// panels compute.  With `parts` > 1 the first panel is computed in two
+// column halves: B comes in those halves (the first panel's rows of A before
+// them), so the first C values start back after half of B instead of all
 // of it.  `prep_b(c0, nc)` enqueues what B's columns [c0, c0 + nc) need once
 // they have arrived; `panel(r0, mp, c0, nc)` enqueues the kernels of C's rows
 // [r0, r0 + mp) x columns [c0, c0 + nc).  Everything is enqueued before the
@@ -747,7 +747,7 @@ gemmpipe_status_t host_call(int dev, cudaStream_t s, int64_t M, int64_t N, int64
 {
     const int64_t rows = gemmpipe_host_panel_rows(M);
     const int64_t P = (M + rows - 1) / rows;
-    const int Q = K > 0 && parts > 1 ? parts : 1;  // column parts of the first panel
+    const int Q = K > 0 && parts > 1 ? 2 : 1;  // column parts of the first panel: one or two (halves)
     const int64_t w = Q > 1 ? N / Q / 16 * 16 : N;   // whole 16-column groups: bases stay on 16 bytes
     const auto col0 = [&](int q) { return q * w; };
     const auto ncol = [&](int q) { return q == Q - 1 ? N - col0(q) : w; };

@@ -23,6 +23,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// SM cycle counter (counts at the SM's current clock).
+__device__ __forceinline__ uint64_t sm_clock64()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+    return t;
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

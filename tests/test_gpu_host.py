@@ -168,13 +168,15 @@ def test_host_s8_other_int8_paths(dev, producer):
     assert np.array_equal(got, oracle.gemm_s8s8s32(A, B))
 
 
-def test_host_s8_full_size_sampled(dev):
+def test_host_s8_full_size(dev, full_size):
     """INT8 4096^3 (four panels of 1024 rows, the first in column halves)
-    through host buffers, checked on sampled rows: the first and last rows of
-    every panel and random ones."""
-    M = N = K = 4096
-    A, B = inputs.workload_operands(2)[5:7]
-    got = run_host("s8", A, B, True)
-    rows = sorted({0, 1, 511, 512, 1023, 1024, 2047, 2048, 3071, 3072, 4095} |
-                  set(int(x) for x in np.random.default_rng(5).integers(0, M, 16)))
-    assert np.array_equal(got[rows], oracle.gemm_s8s8s32(A, B, rows=rows))
+    through host buffers, every element bit for bit."""
+    A, B, want = full_size(2)
+    assert np.array_equal(run_host("s8", A, B, True), want)
+
+
+def test_host_f16_full_size(dev, full_size):
+    """FP16 4096^3 through host buffers (four panels, the first in column
+    halves), every element within the FP16 tolerance."""
+    A, B, want = full_size("fp16_4096")
+    assert_f16_close(run_host("f16", A, B, True), want, "fp16 4096^3 host")

@@ -4,11 +4,8 @@ INT8 results must equal the oracle bit for bit.  FP16 results (fp32
 accumulation on the tensor cores) must be within max-abs 1e-2 and relative
 Frobenius 1e-4 of the oracle's fp64-accumulated product.
 
-Sizes the oracle finishes in seconds are compared element by element, the
-INT8 4096^3 headline included; the full-size FP16 workloads are compared on
-sampled rows (every column of each sampled row, so every column tile
-including the ragged last one), chosen to include the first and last rows of
-M tiles.
+Every test compares every element of C, the full-size workloads included
+(their oracle products are computed once per session, see conftest).
 """
 from __future__ import annotations
 
@@ -252,29 +249,29 @@ def test_workload_fp16_1024(dev):
     assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), "fp16 1024^3")
 
 
-def test_workload_int8_4096(dev):
-    # Every element of the headline workload, bit for bit (the oracle takes
-    # a few seconds on all host cores).
-    _, _, M, N, K, A, B = inputs.workload_operands(2)
+def test_workload_int8_4096(dev, full_size):
+    # Every element of the headline workload, bit for bit.
+    A, B, want = full_size(2)
+    K = A.shape[1]
     got = run_s8(A, B, dev)
-    assert np.array_equal(got, oracle.gemm_s8s8s32(A, B))
+    assert np.array_equal(got, want)
     # Any-size property: int8 products are bounded by 2^14 K.
     assert np.abs(got.astype(np.int64)).max() <= 16384 * K
 
 
-def test_workload_fp16_skinny_sampled(dev):
-    _, _, M, N, K, A, B = inputs.workload_operands(3)
-    got = run_f16(A, B, dev)
-    rows = sample_rows(M)
-    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "skinny")
-    assert np.isfinite(got).all()
+def test_workload_fp16_skinny(dev, full_size):
+    # Every element of the 16384 x 128 C (128 whole tiles, A streamed once).
+    A, B, want = full_size(3)
+    assert_f16_close(run_f16(A, B, dev), want, "skinny")
 
 
 @pytest.mark.parametrize("forced", [-1, 1], ids=["padded_tma", "bounded_loads"])
-def test_workload_fp16_ragged_sampled(dev, forced):
-    _, _, M, N, K, A, B = inputs.workload_operands(4)
-    rows = sample_rows(M)
-    ref = oracle.gemm_f16f32(A, B, rows=rows)
+def test_workload_fp16_ragged(dev, full_size, forced):
+    # Every element of the 4093 x 3001 C: partial last tiles in M, N and K,
+    # most tiles split into k-block ranges over the persistent grid.
+    A, B, want = full_size(4)
+    M, K = A.shape
+    N = B.shape[1]
     gemmpipe.gemmpipe_set_plan_override(forced, 0, 0)
     try:
         plan = gemmpipe.gemmpipe_plan(1, M, N, K)
@@ -282,8 +279,7 @@ def test_workload_fp16_ragged_sampled(dev, forced):
     finally:
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert plan["k_blocks"] == (K + 63) // 64
-    assert_f16_close(got[rows], ref, "ragged")
-    assert np.isfinite(got).all()
+    assert_f16_close(got, want, "ragged")
 
 
 # --------------------------------------------------------- bounded waits
@@ -540,17 +536,16 @@ def test_cta_pair_stall_times_out(dev):
     assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
-def test_workload_fp16_4096_sampled(dev):
-    # The fp16 half of the headline metric: 4096^3, uniform [-1, 1]; the
-    # 256 pair tiles leave a partial last wave, so the last two waves are
-    # split into k-block ranges.
-    M = N = K = 4096
-    A, B = inputs.make_operands("f16", M, N, K, seed=inputs.SEED_BASE + 5)
+def test_workload_fp16_4096(dev, full_size):
+    # The fp16 half of the headline metric: 4096^3, uniform [-1, 1], every
+    # element.  The 256 pair tiles leave a partial last wave, so the last
+    # two waves are split into k-block ranges.
+    A, B, want = full_size("fp16_4096")
+    M, K = A.shape
+    N = B.shape[1]
     plan = gemmpipe.gemmpipe_plan(1, M, N, K)
     assert plan["tiles"] % plan["units"] == 0 or plan["split_tiles"] > 0
-    got = run_f16(A, B, dev)
-    rows = sample_rows(M)
-    assert_f16_close(got[rows], oracle.gemm_f16f32(A, B, rows=rows), "fp16 4096^3")
+    assert_f16_close(run_f16(A, B, dev), want, "fp16 4096^3")
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 272, 1040), (129, 512, 2048), (1000, 256, 4096),

@@ -48,14 +48,14 @@ def traced(dev, stages: int):
     try:
         plan = gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)
         gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)  # warm
-        buf = torch.zeros(2 * N_TRACE, dtype=torch.int64, device=dev)
+        buf = torch.zeros(3 * N_TRACE, dtype=torch.int64, device=dev)
         gemmpipe.gemmpipe_test_trace(buf, N_TRACE)
         gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
         assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
     finally:
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
     t = buf.cpu().numpy()
-    return t[:N_TRACE], t[N_TRACE:], plan
+    return t[:N_TRACE], t[N_TRACE:2 * N_TRACE], t[2 * N_TRACE:], plan
 
 
 def stats(prod, mma):
@@ -71,8 +71,8 @@ def stats(prod, mma):
 
 
 def test_ring_overlaps_loads_with_mma(dev):
-    p6, m6, plan6 = traced(dev, 6)
-    p1, m1, plan1 = traced(dev, 1)
+    p6, m6, c6, plan6 = traced(dev, 6)
+    p1, m1, c1, plan1 = traced(dev, 1)
     assert plan6["stages"] == 6 and plan1["stages"] == 1 and plan6["cta_pair"] == plan1["cta_pair"] == 1
     next6, gap6 = stats(p6, m6)
     next1, gap1 = stats(p1, m1)
@@ -83,3 +83,15 @@ def test_ring_overlaps_loads_with_mma(dev):
     # k-blocks come at least twice as fast.
     assert next6 >= 0.5, next6
     assert gap1 >= 2 * gap6, (gap1, gap6)
+
+
+def test_trace_cycle_stamps_follow_the_clock(dev):
+    """The %clock64 stamps beside the MMA-ready times count SM cycles: they
+    increase with every k-block, and cycles over nanoseconds between the
+    first and last stamp is an SM clock between 0.5 and 2.2 GHz."""
+    prod, mma, cyc, _ = traced(dev, 6)
+    used = int((prod > 0).sum())
+    assert used > 32
+    assert (np.diff(cyc[:used]) > 0).all()
+    ghz = (cyc[used - 1] - cyc[0]) / (mma[used - 1] - mma[0])
+    assert 0.5 <= ghz <= 2.2, ghz
