@@ -313,7 +313,8 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * pages' own design as a comparison path: warp-level integer MMA
  * (mma.sync m16n8k32) fed by a 4-stage cp.async ring, on A and a transposed
  * copy of B in the workspace (N x K bytes); exact like the other paths.  bn: 0
- * automatic, else 128 or 256.  stages: 0 automatic, else one of the compiled
+ * automatic, else 128, 256 or 512 (512: 256 x 512 tiles on CTA pairs, fp16
+ * output only; where that variant does not apply, 256).  stages: 0 automatic, else one of the compiled
  * ring depths (when the chosen variant has no such depth the automatic one
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
  * 0 single CTAs, 1 CTA pairs where the shape allows them.  split: -1
@@ -370,8 +371,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int t
  * Test hook that shows the pipelining ("Pipeline GPU Kernel", Steps 3-4:
  * the loads of the next K-tiles are issued while the tensor cores work on
  * this one).  For the next GEMM launch only, and when that launch runs the
- * FP16 CTA-pair kernel with a 6- or 1-stage ring (the two kernels compiled
- * with the trace; any other launch consumes the hook and records nothing),
+ * FP16 CTA-pair kernel with 256-wide tiles and a 6- or 1-stage ring, or
+ * with 512-wide tiles (the kernels compiled with the trace; any other
+ * launch consumes the hook and records nothing),
  * CTA 0 (the leader CTA of pair 0) writes %globaltimer nanoseconds into `buffer`, a
  * device array of 3 * `entries` uint64: element j (j < entries) when its
  * producer has issued the tile copies of its j-th k-block (counted over the

@@ -72,10 +72,17 @@ struct GemmCfg {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int CTA_BN = PAIR ? BN / 2 : BN;
 
+    // Columns of one tcgen05.mma (N <= 256); a 512-wide pair tile issues
+    // two per k-step into the two halves of one 512-column accumulator.
+    // Each CTA of a pair holds, for every MMA, MMA_N / 2 columns of B.
+    static constexpr int MMA_N = BN < 256 ? BN : 256;
+    static constexpr int N_MMAS = BN / MMA_N;
+
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BK * CTA_BN * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NB64 = CTA_BN / 64;  // 64-column B atoms per stage
+    static constexpr int NB64_PER_MMA = NB64 / N_MMAS;
 
     // CONVERT: int8 operands arrive by TMA in an int8 ring; converter warps
     // widen them to fp16 into the MMA's stage (INT8 path without a widening
@@ -112,7 +119,14 @@ struct GemmCfg {
     // registers each; with more warps they are kept in C itself.
     static constexpr bool SUM_IN_C = CONVERT && THREADS > 12 * 32;
     static constexpr int EPI_COLS = BN / 2;  // columns per epilogue warp
-    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    // Two accumulators (tile t+1's MMAs run while tile t is stored), or
+    // one of 512 columns for the 512-wide pair tile: TMEM holds 512.
+    static constexpr int ACC_BUFS = BN == 512 ? 1 : 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * BN;
+    // The epilogue holds at most 128 accumulator values per thread at a
+    // time: a 512-wide tile's 256 columns per warp go in two passes.
+    static constexpr int EPI_PASS_COLS = EPI_COLS < 128 ? EPI_COLS : 128;
+    static constexpr int EPI_PASSES = EPI_COLS / EPI_PASS_COLS;
 
     static constexpr int I8_OFF = STAGES * STAGE_BYTES;
     static constexpr int STAGING_OFF = I8_OFF + I8_STAGES * I8_STAGE_BYTES;
@@ -121,11 +135,13 @@ struct GemmCfg {
     static constexpr int CTL_BYTES = 8 * (2 * STAGES + 2 * I8_STAGES + 5) + 16;
     static constexpr int SMEM_BYTES = 1024 + CTL_OFF + CTL_BYTES;  // + alignment slack
 
-    static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    static_assert(BN == 128 || BN == 256 || BN == 512, "BN must be 128, 256 or 512");
+    static_assert(BN != 512 || (PAIR && !INT_OUT && !CONVERT),
+                  "512-wide tiles: fp16 CTA pairs only (the INT8 epilogue keeps 128 int32 sums per thread)");
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
-    static_assert(!PAIR || (BN == 256 && !LDG), "pair variant: TMA producer, 256-wide tiles");
+    static_assert(!PAIR || (BN >= 256 && !LDG), "pair variant: TMA producer, 256- or 512-wide tiles");
     static_assert(!CONVERT || I8_B_ATOMS >= 1, "int8 B atoms are 128 columns wide");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
@@ -676,7 +692,9 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     Work wk;
     while (ok && it.next(p, wk)) {
         const int32_t m0 = static_cast<int32_t>(wk.m0 + rank * Cfg::BM);
-        const int32_t n0 = static_cast<int32_t>(wk.n0 + rank * Cfg::CTA_BN);  // this CTA's half of B
+        // This CTA's share of B: for each MMA of the k-step, its half of
+        // that MMA's MMA_N columns.
+        const int32_t n0 = static_cast<int32_t>(wk.n0 + rank * (Cfg::MMA_N / 2));
         for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
                 ok = false;
@@ -690,7 +708,9 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
                 tma_load_2d_pair(sa, tA, fb, k0, m0);
 #pragma unroll
-                for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                for (int j = 0; j < Cfg::NB64; ++j)
+                    tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb,
+                                     n0 + (j / Cfg::NB64_PER_MMA) * Cfg::MMA_N + 64 * (j % Cfg::NB64_PER_MMA), k0);
                 if constexpr (Cfg::TRACE) {
                     if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
                 }
@@ -733,8 +753,10 @@ template <class Cfg>
 __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
                                 Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
-    constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::BN, true);
+    constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::MMA_N, true);
     constexpr uint16_t BOTH = 3;
+    // Byte offset of the B columns of MMA u of a k-step within a stage's B.
+    constexpr int B_MMA_BYTES = Cfg::NB64_PER_MMA * 8192;
     // Per-stage, per-k-step descriptors are offsets of these two (see mma_issuer).
     const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);
     const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, 8192, 1024);
@@ -768,10 +790,13 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                 }
                 tc_fence_after_sync();
                 const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
-                umma_f16_pair(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
 #pragma unroll
-                for (int kk = 1; kk < Cfg::BK / 16; ++kk)
-                    umma_f16_pair(d, dA0 + so + (kk * 32 >> 4), dB0 + so + (kk * 2048 >> 4), idesc, 1u);
+                for (int kk = 0; kk < Cfg::BK / 16; ++kk)
+#pragma unroll
+                    for (int u = 0; u < Cfg::N_MMAS; ++u)
+                        umma_f16_pair(d + u * Cfg::MMA_N, dA0 + so + (kk * 32 >> 4),
+                                      dB0 + so + ((u * B_MMA_BYTES + kk * 2048) >> 4), idesc,
+                                      (kb > kc || kk > 0) ? 1u : 0u);
                 issued = true;
                 umma_commit_pair(smem_u32(&ctl->empty[stage]), BOTH);
                 if (++stage == Cfg::STAGES) {
@@ -781,17 +806,22 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
             }
             if (!ok) break;
             umma_commit_pair(smem_u32(&ctl->tfull[acc]), BOTH);
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            if constexpr (Cfg::ACC_BUFS == 2) {
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            } else {
+                acc_phase ^= 1u;
+            }
         }
     }
     if (ok) {
-        // Both accumulators' last releases -- including the peer's
+        // The accumulators' last releases -- including the peer's
         // epilogue arrivals on these barriers -- have landed before the
         // pair's final (relaxed) cluster barrier.  The parities are the
         // ones the next use of each buffer would wait for.
-        ok = w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u) &&
-             w.wait(smem_u32(&ctl->tempty[acc ^ 1u]), acc == 0 ? acc_phase ^ 1u : acc_phase);
+        ok = w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u);
+        if constexpr (Cfg::ACC_BUFS == 2)
+            ok = ok && w.wait(smem_u32(&ctl->tempty[acc ^ 1u]), acc == 0 ? acc_phase ^ 1u : acc_phase);
     }
     if (!ok && issued) {
         umma_commit_pair(smem_u32(&ctl->drain), 1);
@@ -1030,6 +1060,13 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
     // global traffic, so the MMA never waits on C stores or partial sums.
     // Otherwise it works one 32-column block at a time.
     constexpr bool HOLD = Cfg::REG_SPLIT && !INT;
+    // A 512-wide tile gives each warp 256 columns: too many to hold.  It
+    // copies them in passes of 128 and frees the accumulator after the last
+    // pass's copy; the MMA of the next item waits for the earlier passes'
+    // stores (this tile shape has no second accumulator to overlap with).
+    constexpr bool HOLD_N = HOLD && Cfg::EPI_PASSES > 1;
+    constexpr bool HOLD_1 = HOLD && !HOLD_N;
+    constexpr int NBP = Cfg::EPI_PASS_COLS / 32;  // 32-column blocks per pass
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
     const int64_t me = unit_index<Cfg>();
     const int64_t my_slot = slot_of<Cfg>(me, rank);
@@ -1044,8 +1081,12 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
             else
                 mbar_arrive(smem_u32(&ctl->tempty[acc]));
         }
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if constexpr (Cfg::ACC_BUFS == 2) {
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        } else {
+            acc_phase ^= 1u;
+        }
     };
     // The other parts of a split tile must be published before they are
     // added.  Each is the first split item of a lower unit, which waits on
@@ -1063,8 +1104,9 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
         const int64_t row0 = wk.m0 + rank * Cfg::BM + q * 32;
         const int64_t colb = wk.n0 + h * NCOLS;
         const int64_t v_lo = wk.kind == 2 ? first_part_unit<Cfg>(p, wk.sk_tile) : me;
-        if (!HOLD && !ISUM && wk.kind == 2 && !wait_parts(v_lo)) return;
-        uint32_t val[(HOLD || ISUM) ? NCOLS : 1];  // fp32 bits (HOLD) or int32 sums (ISUM)
+        if ((!HOLD || HOLD_N) && !ISUM && wk.kind == 2 && !wait_parts(v_lo)) return;
+        // fp32 bits (HOLD) or int32 sums (ISUM)
+        uint32_t val[(HOLD_1 || ISUM) ? NCOLS : (HOLD_N ? Cfg::EPI_PASS_COLS : 1)];
         if constexpr (ISUM) {
 #pragma unroll
             for (int i = 0; i < NCOLS; ++i) val[i] = 0;
@@ -1104,11 +1146,34 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                     for (int i = 0; i < 32; ++i)
                         val[jb * 32 + i] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
                 }
-            } else if constexpr (HOLD) {
+            } else if constexpr (HOLD_1) {
 #pragma unroll
                 for (int jb = 0; jb < NB; ++jb)
                     tmem_ld_32x32b_x32(tbase + jb * 32, *reinterpret_cast<uint32_t(*)[32]>(&val[jb * 32]));
                 tmem_wait_ld();
+            } else if constexpr (HOLD_N) {
+                // One accumulation per item (fp32 output).  The other parts
+                // of a split tile were awaited at the start of the item.
+#pragma unroll 1
+                for (int ps = 0; ps < Cfg::EPI_PASSES; ++ps) {
+#pragma unroll
+                    for (int jb = 0; jb < NBP; ++jb)
+                        tmem_ld_32x32b_x32(tbase + ps * Cfg::EPI_PASS_COLS + jb * 32,
+                                           *reinterpret_cast<uint32_t(*)[32]>(&val[jb * 32]));
+                    tmem_wait_ld();
+                    if (ps == Cfg::EPI_PASSES - 1) release();
+#pragma unroll
+                    for (int jb = 0; jb < NBP; ++jb) {
+                        const int b = ps * NBP + jb;
+                        if (wk.kind == 1) {
+                            write_part(part_block<Cfg>(p, my_slot, e, b), &val[jb * 32], lane);
+                        } else {
+                            for (int64_t v = me - 1; v >= v_lo; --v)
+                                add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, b), &val[jb * 32], lane);
+                            store_block(p, tC, stg, &val[jb * 32], row0, colb + b * 32, lane);
+                        }
+                    }
+                }
             } else {
 #pragma unroll
                 for (int jb = 0; jb < NB; ++jb) {
@@ -1124,9 +1189,9 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                     }
                 }
             }
-            release();
+            if constexpr (!HOLD_N) release();
         }
-        if constexpr (ISUM || HOLD) {
+        if constexpr (ISUM || HOLD_1) {
             // The accumulator is already free.  A split tile's other parts
             // are added in unit order (exact for integers; a fixed order for
             // fp32), then the slice goes to C or to this unit's slot.

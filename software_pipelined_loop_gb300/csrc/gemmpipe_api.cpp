@@ -252,18 +252,23 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (int_out) producer = 0;  // widened operands are always TMA-describable
     int bn = N <= 128 ? 128 : 256;
     if (ov.bn) bn = ov.bn;
-    // A CTA pair (256 x 256 tiles, cta_group::2 MMA) when both dimensions
-    // exceed one 128-row / 128-column tile and TMA reads the operands.
+    // A CTA pair (256 x 256 or 256 x 512 tiles, cta_group::2 MMA) when both
+    // dimensions exceed one 128-row / 128-column tile and TMA reads the
+    // operands.  512-wide tiles exist for fp16 output only; elsewhere they
+    // become 256-wide.
     const Variant *v = nullptr;
-    if (producer == 0 && bn == 256 && M > kBM && N > 128 && ov.pair != 0) {
-        v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
+    if (producer == 0 && bn >= 256 && M > kBM && N > 128 && ov.pair != 0) {
+        v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
+        if (!v && bn == 512) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;
     }
+    if (bn == 512 && (!v || !v->info.pair)) bn = 256;
     if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages, 0);
     if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, 0, 0);
     if (!v) return GEMMPIPE_ERR_INTERNAL;
     if (v->info.smem_bytes > d.smem_optin) return GEMMPIPE_ERR_UNSUPPORTED_DEVICE;
     pl->v = v;
+    bn = v->info.BN;
     const int64_t tile_m = v->info.pair ? 2 * kBM : kBM;
     pl->m_tiles = (M + tile_m - 1) / tile_m;
     pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
@@ -1209,7 +1214,7 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
 gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair, int split)
 {
     if (producer < -1 || producer > 2) return GEMMPIPE_ERR_INVALID_VALUE;
-    if (bn != 0 && bn != 128 && bn != 256) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (bn != 0 && bn != 128 && bn != 256 && bn != 512) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
     if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     if (split < -1 || split > 1) return GEMMPIPE_ERR_INVALID_VALUE;

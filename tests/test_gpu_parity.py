@@ -703,3 +703,60 @@ def test_extreme_aspect_ratios(dev, dtype, M, N, K):
         assert np.array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
     else:
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B), f"{M}x{N}x{K}")
+
+
+# ------------------------------------------------- 512-wide CTA-pair tiles
+
+@pytest.mark.parametrize("split", [-1, 0, 1], ids=["auto", "whole", "split"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 64),        # one tile, one k-block
+                                   (520, 1030, 1000),     # ragged M, N, K; several tiles
+                                   (300, 600, 4107),      # two column tiles, the second mostly empty
+                                   (1024, 2048, 2048),    # more tiles than one pass of each pair
+                                   (2000, 3000, 257)])    # ragged everything, 5 k-blocks
+def test_bn512_pair_tiles(dev, M, N, K, split):
+    # 256 x 512 tiles: two N = 256 MMAs per k-step into one 512-column
+    # accumulator, drained in two passes; whole tiles and stream-K splits.
+    A, B = inputs.make_operands("f16", M, N, K, seed=900 + M + N + K)
+    gemmpipe.gemmpipe_set_plan_override(-1, 512, 0, 1, split)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert plan["BN"] == 512 and plan["cta_pair"] == 1 and plan["stages"] == 4
+        if split == 0:
+            assert plan["split_tiles"] == 0
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    assert_f16_close(got, oracle.gemm_f16f32(A, B), f"{M}x{N}x{K} split={split}")
+
+
+def test_bn512_falls_back_for_int8_and_narrow_shapes(dev):
+    # No 512-wide INT8 variant (its epilogue keeps int32 sums per thread)
+    # and no pair for a single row tile: the override then takes 256.
+    gemmpipe.gemmpipe_set_plan_override(-1, 512, 0, -1, -1)
+    try:
+        assert gemmpipe.gemmpipe_plan(0, 1024, 1024, 1024)["BN"] == 256
+        p = gemmpipe.gemmpipe_plan(1, 100, 1024, 256)
+        assert p["BN"] == 256 and p["cta_pair"] == 0
+        A, B = inputs.make_operands("s8", 300, 700, 300, seed=931)
+        np.testing.assert_array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+
+
+def test_bn512_stall_times_out(dev):
+    import torch
+    M, N, K = 512, 1024, 1024
+    A, B = inputs.make_operands("f16", M, N, K, seed=933)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    gemmpipe.gemmpipe_set_plan_override(-1, 512, 0, 1, -1)
+    try:
+        assert gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)["BN"] == 512
+        gemmpipe.gemmpipe_test_inject_stall(2, 200)
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
