@@ -707,10 +707,20 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
                 tma_load_2d_pair(sa, tA, fb, k0, m0);
+                if (p.b_groups) {
+                    // One 3-D copy per MMA: its NB64_PER_MMA 64-column groups,
+                    // 8 KiB apart in shared memory as the 2-D copies place them.
 #pragma unroll
-                for (int j = 0; j < Cfg::NB64; ++j)
-                    tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb,
-                                     n0 + (j / Cfg::NB64_PER_MMA) * Cfg::MMA_N + 64 * (j % Cfg::NB64_PER_MMA), k0);
+                    for (int u = 0; u < Cfg::N_MMAS; ++u)
+                        tma_load_3d_pair(sa + Cfg::A_BYTES + u * Cfg::NB64_PER_MMA * 8192, tB, fb, 0, k0,
+                                         (n0 + u * Cfg::MMA_N) / 64);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < Cfg::NB64; ++j)
+                        tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb,
+                                         n0 + (j / Cfg::NB64_PER_MMA) * Cfg::MMA_N + 64 * (j % Cfg::NB64_PER_MMA),
+                                         k0);
+                }
                 if constexpr (Cfg::TRACE) {
                     if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
                 }

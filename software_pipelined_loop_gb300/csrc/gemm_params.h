@@ -36,6 +36,10 @@ struct GemmParams {
     int64_t kb_per_chunk;  // k-blocks per TMEM accumulation unit
     int vec_store;         // C base and pitch allow 16-byte stores
     int tma_store;         // C blocks leave through TMA bulk-tensor stores (the C tensor map is valid)
+    // B's tensor map is 3-D (64 columns x K rows x N / 64 column groups):
+    // one copy brings a CTA's whole share of a B k-block (CTA pairs, N a
+    // multiple of 64); otherwise 2-D, one copy per 64 columns.
+    int b_groups = 0;
     int64_t stall_kb;      // test hook: CTA 0 leaves this k-block unfilled (-1: none)
     // Test hook: CTA 0 (the leader of pair 0) stamps %globaltimer into
     // trace[j] when its producer has issued the copies of its j-th k-block

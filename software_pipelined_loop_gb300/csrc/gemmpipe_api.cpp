@@ -371,6 +371,24 @@ bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int
     return encode_2d_any(m, base, rows, cols, ld, 64, box_rows, false);
 }
 
+// B (rows x cols fp16, pitch ld, cols a multiple of 64) as 64 columns x
+// rows x cols / 64 column groups, 128-byte swizzle; a box of box_rows rows
+// and `groups` column groups lands as `groups` 64-column atoms, 8 KiB apart
+// for 64-row boxes -- the layout of that many 2-D boxes.
+bool encode_b_groups(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                     int groups)
+{
+    EncodeFn f = encode_fn();
+    if (!f || cols % 64 != 0) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(groups)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // C (rows x cols of 4-byte elements, pitch ld) for the epilogue's TMA
 // stores: 32 x 32 boxes in the 128-byte swizzle of its staging tiles.
 bool encode_c(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld, bool int_out)
@@ -514,6 +532,7 @@ void set_schedule(Plan &pl, int dev, cudaStream_t s, GemmParams &p)
 gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, const uint16_t *A, int64_t lda,
                            const uint16_t *B, int64_t ldb, void *C, int64_t ldc, cudaStream_t s)
 {
+    int b_groups = 0;
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
@@ -525,8 +544,12 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
             return GEMMPIPE_ERR_INTERNAL;
     } else if (pl.v->info.producer == 0) {
         // Boxes: A 64 (k) x 128 rows, B 64 (n) x 64 (k); a pair CTA loads the
-        // same boxes for its half.
-        if (!encode_2d(&ta, A, M, K, lda, kBM) || !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
+        // same boxes for its half -- or, when N is a multiple of 64, each
+        // MMA's share of B in one 3-D box of 64-column groups.
+        if (!encode_2d(&ta, A, M, K, lda, kBM)) return GEMMPIPE_ERR_INTERNAL;
+        const int per_mma = pl.v->info.BN / (pl.v->info.BN > 256 ? pl.v->info.BN / 256 : 1) / 2 / 64;
+        b_groups = pl.v->info.pair && N % 64 == 0 && encode_b_groups(&tb, B, K, N, ldb, kBK, per_mma) ? 1 : 0;
+        if (!b_groups && !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
     }
     CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
@@ -541,6 +564,7 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
     p.C = C;
     p.ldc = ldc;
     set_schedule(pl, dev, s, p);
+    p.b_groups = b_groups;
     p.tma_store = pl.vec_store && encode_c(&tc, C, M, N, ldc, pl.v->info.int_out != 0) ? 1 : 0;
     p.stall_kb = -1;
     p.timeout_ns = 2000000000ull + static_cast<uint64_t>(pl.kb_per_chunk) * 10000ull;
