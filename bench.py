@@ -69,13 +69,14 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of a kernel variant, from one
 # `ncu --set full` capture of that launch, valid only while the kernel
 # sources hash as they did when the counters were taken (else null).
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu"]
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu",
+                  "gemmpipe_api.cpp"]
 TRAFFIC = {
     # (dtype, M, N, K, cta pair, BN): (bytes per launch, sources hash)
-    ("s8", 4096, 4096, 4096, 1, 256): (139_024_640, "b8ac23c89f1e0055"),
-    ("f16", 4096, 4096, 4096, 1, 256): (139_781_120, "b8ac23c89f1e0055"),
-    ("f16", 16384, 128, 16384, 0, 128): (544_346_880, "b8ac23c89f1e0055"),
-    ("f16", 4093, 3001, 4107, 1, 256): (112_088_064, "b8ac23c89f1e0055"),
+    ("s8", 4096, 4096, 4096, 1, 256): (138_304_000, "8e62c5d61b061468"),
+    ("f16", 4096, 4096, 4096, 1, 256): (138_573_824, "8e62c5d61b061468"),
+    ("f16", 16384, 128, 16384, 0, 128): (544_323_584, "8e62c5d61b061468"),
+    ("f16", 4093, 3001, 4107, 1, 256): (111_441_920, "8e62c5d61b061468"),
 }
 
 

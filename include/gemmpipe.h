@@ -277,7 +277,9 @@ typedef struct {
     int stages;          /* depth S of the shared-memory ring */
     int k_chunk;         /* k values accumulated in one TMEM accumulator before a drain */
     int threads;         /* threads per CTA */
-    int cta_pair;        /* 1: clusters of two CTAs share one 256-row MMA (tcgen05 cta_group::2) */
+    int cta_pair;        /* 1: clusters of two CTAs share one 256-row MMA (tcgen05 cta_group::2);
+                            2: quads, two such pairs per cluster sharing A (BN is then the
+                            quad's tile width, 512) */
     int grid;            /* persistent CTAs launched */
     int64_t tiles;       /* output tiles of BM x BN */
     int64_t units;       /* persistent units: CTAs, or CTA pairs */
@@ -317,7 +319,10 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * output only; where that variant does not apply, 256).  stages: 0 automatic, else one of the compiled
  * ring depths (when the chosen variant has no such depth the automatic one
  * is used; gemmpipe_plan reports what was taken).  cta_pair: -1 automatic,
- * 0 single CTAs, 1 CTA pairs where the shape allows them.  split: -1
+ * 0 single CTAs, 1 CTA pairs where the shape allows them, 2 quads (a
+ * cluster of two CTA pairs computing a 256 x 512 tile; each CTA loads half
+ * of its rows of A and multicasts it to its counterpart in the other pair)
+ * where the shape allows them.  split: -1
  * automatic, 0 every tile whole (no stream-K split), 1 split wherever the
  * schedule can (also where the automatic rule keeps whole tiles: a nearly
  * full last wave, a modest cut in k-blocks per CTA, memory-bound shapes

@@ -6,6 +6,8 @@ namespace gp {
 static const Variant kF16Variants[] = {
     make_variant<GemmCfg<256, 4, false, false>>(),  // TMA producer, 128x256 tiles
     make_variant<GemmCfg<256, 6, false, false, false, 1, true>>(),  // CTA pair, 256x256 tiles
+    // Quad: two CTA pairs (256x512 tile) sharing A by multicast.
+    make_variant<GemmCfg<256, 6, false, false, false, 1, true, 1, 4, false, true>>(),
     // CTA pair, 256x512 tiles: two N = 256 MMAs per k-step into one
     // 512-column accumulator; 48 B of operands per MMA cycle per SM instead
     // of 64, under what an SM can take in.
@@ -25,6 +27,7 @@ static const Variant kF16Variants[] = {
     make_variant<GemmCfg<256, 6, false, false, false, 1, true, 1, 4, true>>(),
     make_variant<GemmCfg<256, 1, false, false, false, 1, true, 1, 4, true>>(),
     make_variant<GemmCfg<512, 4, false, false, false, 1, true, 1, 4, true>>(),
+    make_variant<GemmCfg<256, 6, false, false, false, 1, true, 1, 4, true, true>>(),
 };
 
 int variants_f16(const Variant **out)

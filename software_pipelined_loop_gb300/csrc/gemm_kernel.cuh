@@ -53,7 +53,7 @@ namespace gp {
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
 template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1,
-          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4, bool TRACE_ = false>
+          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4, bool TRACE_ = false, bool QUAD_ = false>
 struct GemmCfg {
     // TRACE: a copy of the kernel that stamps the pipelining trace (the
     // test hook gemmpipe_test_trace); the others carry no trace code.
@@ -71,6 +71,15 @@ struct GemmCfg {
     static constexpr bool PAIR = PAIR_;
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int CTA_BN = PAIR ? BN / 2 : BN;
+    // QUAD: a cluster of two CTA pairs computes a 256 x 2BN tile, each pair
+    // its own BN columns over the same 256 rows.  The pairs share A: each
+    // CTA loads half of its 128 rows of a k-block and multicasts it to its
+    // counterpart in the other pair, so an SM issues 24 KiB of copies per
+    // k-block instead of 32 (copy issue per SM, not data arriving, is what
+    // bounds the k-loop).
+    static constexpr bool QUAD = QUAD_;
+    static constexpr int CLUSTER = QUAD ? 4 : (PAIR ? 2 : 1);
+    static constexpr int TILE_N = QUAD ? 2 * BN : BN;
 
     // Columns of one tcgen05.mma (N <= 256); a 512-wide pair tile issues
     // two per k-step into the two halves of one 512-column accumulator.
@@ -142,6 +151,7 @@ struct GemmCfg {
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
     static_assert(!PAIR || (BN >= 256 && !LDG), "pair variant: TMA producer, 256- or 512-wide tiles");
+    static_assert(!QUAD || (PAIR && BN == 256 && !CONVERT), "quad variant: two CTA pairs of 256 x 256 tiles");
     static_assert(!CONVERT || I8_B_ATOMS >= 1, "int8 B atoms are 128 columns wide");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(SMEM_BYTES <= 232448, "over the per-CTA shared-memory limit");
@@ -243,7 +253,7 @@ struct Work {
 template <class Cfg>
 __device__ __forceinline__ int64_t unit_index()
 {
-    return Cfg::PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+    return blockIdx.x / Cfg::CLUSTER;
 }
 
 // Start of a unit's range of split k-blocks (units[u] covers
@@ -308,7 +318,7 @@ struct WorkIter {
         const uint32_t gm = mt - first < gmax ? mt - first : gmax;
         const uint32_t col = in / gm;
         w.m0 = static_cast<int64_t>(first + (in - col * gm)) * Cfg::TILE_M;
-        w.n0 = static_cast<int64_t>(col) * Cfg::BN;
+        w.n0 = static_cast<int64_t>(col) * Cfg::TILE_N;
         return true;
     }
 };
@@ -677,7 +687,7 @@ __device__ void producer_ldg(const GemmParams &p, uint32_t sbase, Ctl<Cfg::STAGE
 template <class Cfg>
 __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
                                   uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w,
-                                  uint32_t rank)
+                                  uint32_t crank)
 {
     int stage = 0;
     uint32_t phase = 0;
@@ -685,16 +695,22 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     int64_t kb_count = 0;
     bool ok = true;
     constexpr uint32_t pair_bytes = 2u * Cfg::STAGE_BYTES;  // both CTAs' copies
+    const uint32_t rank = crank & 1u;       // rank within the CTA pair
+    const uint32_t pair_i = crank >> 1;     // pair within a quad
+    const uint32_t leader = crank & ~1u;    // cluster rank of the pair's leader
     const bool stall_cta = blockIdx.x == 0 && p.stall_kb >= 0;
     const uint32_t full0 = smem_u32(&ctl->full[0]);
-    const uint32_t full0_leader = mapa_shared(full0, 0);
+    const uint32_t full0_leader = mapa_shared(full0, leader);
+    // Quads: this CTA's half of its A rows goes to it and to its counterpart
+    // in the other pair (same rank within its pair).
+    [[maybe_unused]] const uint16_t a_mask = static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u)));
     WorkIter<Cfg> it(p);
     Work wk;
     while (ok && it.next(p, wk)) {
         const int32_t m0 = static_cast<int32_t>(wk.m0 + rank * Cfg::BM);
         // This CTA's share of B: for each MMA of the k-step, its half of
-        // that MMA's MMA_N columns.
-        const int32_t n0 = static_cast<int32_t>(wk.n0 + rank * (Cfg::MMA_N / 2));
+        // that MMA's MMA_N columns (a quad's second pair: the next BN).
+        const int32_t n0 = static_cast<int32_t>(wk.n0 + pair_i * Cfg::BN + rank * (Cfg::MMA_N / 2));
         for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
             if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
                 ok = false;
@@ -706,7 +722,11 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
-                tma_load_2d_pair(sa, tA, fb, k0, m0);
+                if constexpr (Cfg::QUAD)
+                    tma_load_2d_pair_mc(sa + pair_i * (Cfg::A_BYTES / 2), tA, fb, k0,
+                                        m0 + static_cast<int32_t>(pair_i) * (Cfg::BM / 2), a_mask);
+                else
+                    tma_load_2d_pair(sa, tA, fb, k0, m0);
                 if (p.b_groups) {
                     // One 3-D copy per MMA: its NB64_PER_MMA 64-column groups,
                     // 8 KiB apart in shared memory as the 2-D copies place them.
@@ -758,13 +778,16 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     }
 }
 
-// Leader CTA only: one thread issues the pair's MMAs.
+// Leader CTA only (cluster rank `crank`, even): one thread issues the
+// pair's MMAs.  A stage is released to both CTAs of the pair -- and in a
+// quad to the other pair too, whose A copies also land in these stages.
 template <class Cfg>
 __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
-                                Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
+                                Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, uint32_t crank)
 {
     constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::MMA_N, true);
-    constexpr uint16_t BOTH = 3;
+    const uint16_t BOTH = static_cast<uint16_t>(3u << crank);              // this pair's two CTAs
+    const uint16_t STAGE_MASK = Cfg::QUAD ? static_cast<uint16_t>(0xF) : BOTH;  // whoever writes the stages
     // Byte offset of the B columns of MMA u of a k-step within a stage's B.
     constexpr int B_MMA_BYTES = Cfg::NB64_PER_MMA * 8192;
     // Per-stage, per-k-step descriptors are offsets of these two (see mma_issuer).
@@ -808,7 +831,7 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                                       dB0 + so + ((u * B_MMA_BYTES + kk * 2048) >> 4), idesc,
                                       (kb > kc || kk > 0) ? 1u : 0u);
                 issued = true;
-                umma_commit_pair(smem_u32(&ctl->empty[stage]), BOTH);
+                umma_commit_pair(smem_u32(&ctl->empty[stage]), STAGE_MASK);
                 if (++stage == Cfg::STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -834,7 +857,7 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
             ok = ok && w.wait(smem_u32(&ctl->tempty[acc ^ 1u]), acc == 0 ? acc_phase ^ 1u : acc_phase);
     }
     if (!ok && issued) {
-        umma_commit_pair(smem_u32(&ctl->drain), 1);
+        umma_commit_pair(smem_u32(&ctl->drain), static_cast<uint16_t>(1u << crank));
         w.wait_drain(smem_u32(&ctl->drain), 0, kDrainNs);
     }
 }
@@ -1013,9 +1036,9 @@ __device__ __forceinline__ uint4 *part_block(const GemmParams &p, int64_t slot, 
 }
 
 template <class Cfg>
-__device__ __forceinline__ int64_t slot_of(int64_t unit, uint32_t rank)
+__device__ __forceinline__ int64_t slot_of(int64_t unit, uint32_t crank)
 {
-    return Cfg::PAIR ? 2 * unit + rank : unit;
+    return Cfg::CLUSTER * unit + crank;
 }
 
 __device__ __forceinline__ void write_part(uint4 *blk, const uint32_t *r, int lane)
@@ -1056,8 +1079,11 @@ __device__ __forceinline__ int64_t first_part_unit(const GemmParams &p, int64_t 
 
 template <class Cfg>
 __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sbase, uint32_t tmem_base,
-                         Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, int warp, int lane, uint32_t rank)
+                         Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, int warp, int lane, uint32_t crank)
 {
+    const uint32_t rank = crank & 1u;     // rank within the CTA pair
+    const uint32_t pair_i = crank >> 1;   // pair within a quad
+    const uint32_t leader = crank & ~1u;  // cluster rank of the pair's leader
     const int e = warp - Cfg::EPI_WARP0;  // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int h = e >> 2;                  // column half of the tile
@@ -1079,7 +1105,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
     constexpr int NBP = Cfg::EPI_PASS_COLS / 32;  // 32-column blocks per pass
     const uint32_t stg = sbase + Cfg::STAGING_OFF + e * (32 * 128);
     const int64_t me = unit_index<Cfg>();
-    const int64_t my_slot = slot_of<Cfg>(me, rank);
+    const int64_t my_slot = slot_of<Cfg>(me, crank);
     uint32_t acc = 0, acc_phase = 0;
 
     auto release = [&]() {
@@ -1087,7 +1113,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
         __syncwarp();
         if (lane == 0) {
             if constexpr (Cfg::PAIR)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0));  // the leader's
+                mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), leader));  // the leader's
             else
                 mbar_arrive(smem_u32(&ctl->tempty[acc]));
         }
@@ -1104,7 +1130,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
     auto wait_parts = [&](int64_t v_lo) -> bool {
         bool got = true;
         for (int64_t v = me - 1; v >= v_lo && got; --v)
-            got = w.wait_flag(&p.flags[slot_of<Cfg>(v, rank) * Cfg::EPI_WARPS + e], p.epoch);
+            got = w.wait_flag(&p.flags[slot_of<Cfg>(v, crank) * Cfg::EPI_WARPS + e], p.epoch);
         return __all_sync(0xffffffffu, got);
     };
 
@@ -1112,7 +1138,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
     Work wk;
     while (it.next(p, wk)) {
         const int64_t row0 = wk.m0 + rank * Cfg::BM + q * 32;
-        const int64_t colb = wk.n0 + h * NCOLS;
+        const int64_t colb = wk.n0 + pair_i * Cfg::BN + h * NCOLS;
         const int64_t v_lo = wk.kind == 2 ? first_part_unit<Cfg>(p, wk.sk_tile) : me;
         if ((!HOLD || HOLD_N) && !ISUM && wk.kind == 2 && !wait_parts(v_lo)) return;
         // fp32 bits (HOLD) or int32 sums (ISUM)
@@ -1179,7 +1205,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                             write_part(part_block<Cfg>(p, my_slot, e, b), &val[jb * 32], lane);
                         } else {
                             for (int64_t v = me - 1; v >= v_lo; --v)
-                                add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, b), &val[jb * 32], lane);
+                                add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, crank), e, b), &val[jb * 32], lane);
                             store_block(p, tC, stg, &val[jb * 32], row0, colb + b * 32, lane);
                         }
                     }
@@ -1194,7 +1220,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                         write_part(part_block<Cfg>(p, my_slot, e, jb), r, lane);
                     } else {
                         for (int64_t v = me - 1; v >= v_lo; --v)
-                            add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), r, lane);
+                            add_part<false>(part_block<Cfg>(p, slot_of<Cfg>(v, crank), e, jb), r, lane);
                         store_block(p, tC, stg, r, row0, colb + jb * 32, lane);
                     }
                 }
@@ -1210,7 +1236,7 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                 for (int64_t v = me - 1; v >= v_lo; --v)
 #pragma unroll
                     for (int jb = 0; jb < NB; ++jb)
-                        add_part<INT>(part_block<Cfg>(p, slot_of<Cfg>(v, rank), e, jb), &val[jb * 32], lane);
+                        add_part<INT>(part_block<Cfg>(p, slot_of<Cfg>(v, crank), e, jb), &val[jb * 32], lane);
             }
 #pragma unroll
             for (int jb = 0; jb < NB; ++jb) {
@@ -1248,7 +1274,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]),
                       Cfg::LDG ? Cfg::PRODUCER_THREADS : (Cfg::CONVERT ? (Cfg::PAIR ? 2 : 1) : 1));
-            mbar_init(smem_u32(&ctl->empty[s]), 1);
+            // A quad's stages are written by both pairs' copies: released by both MMA threads.
+            mbar_init(smem_u32(&ctl->empty[s]), Cfg::QUAD ? 2 : 1);
         }
         for (int s = 0; s < Cfg::I8_STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full_i8[s]), 1);
@@ -1288,7 +1315,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     pdl_wait();
     pdl_launch_dependents();
     const Waiter w{&ctl->abort, p.status, p.timeout_ns};
-    const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;
+    const uint32_t rank = Cfg::PAIR ? cluster_ctarank() : 0u;  // rank in the cluster (pair, or quad)
+    const bool pair_leader = (rank & 1u) == 0;
     if constexpr (Cfg::REG_SPLIT) {
         // Each role runs inside the branch that set its register share.
         if (warp < 4) {
@@ -1302,7 +1330,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             } else if (warp == Cfg::MMA_WARP) {
                 if constexpr (Cfg::PAIR) {
-                    if (lane == 0 && rank == 0) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w);
+                    if (lane == 0 && pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank);
                 } else {
                     if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
                 }
@@ -1324,7 +1352,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if constexpr (Cfg::CONVERT) converter<Cfg>(p, sbase, ctl, w);
     } else if (warp == Cfg::MMA_WARP) {
         if constexpr (Cfg::PAIR) {
-            if (lane == 0 && rank == 0) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w);
+            if (lane == 0 && pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank);
         } else {
             if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
         }

@@ -140,14 +140,16 @@ struct Plan {
     int64_t units = 0, dp_tiles = 0, sk_tiles = 0;
     int64_t slots = 0;  // co-resident units (CTAs or CTA pairs)
     int vec_store = 0;
-    int64_t split_ctas() const { return v->info.pair ? 2 * units : units; }
+    // CTAs per unit: 1, a CTA pair (2), or a quad of two pairs (4).
+    int cluster() const { return v->info.pair == 2 ? 4 : (v->info.pair ? 2 : 1); }
+    int64_t split_ctas() const { return cluster() * units; }
     int64_t split_bytes() const;  // stream-K partials + flags (0: none)
     void run_whole_tiles()
     {
         units = tiles < slots ? tiles : slots;
         dp_tiles = tiles;
         sk_tiles = 0;
-        grid = static_cast<int>(v->info.pair ? 2 * units : units);
+        grid = static_cast<int>(cluster() * units);
     }
 };
 
@@ -251,6 +253,15 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (ov.producer == 1) producer = 1;
     if (int_out) producer = 0;  // widened operands are always TMA-describable
     int bn = N <= 128 ? 128 : 256;
+    // Small problems: when the 256 x 256 pair tiles would number at most a
+    // quarter of the SM pairs, single CTAs on 128 x 128 tiles spread the
+    // same k-loop over four times as many SMs with a quarter of the
+    // epilogue each (measured on GB300, L2 flushed, per step: INT8 512^3
+    // 14.6 vs 17.4 us, FP16 512^3 11.5 vs 14.4, FP16 1024^3 14.3 vs 16.6,
+    // INT8 1024^3 17.2 vs 18.4).
+    const int64_t pair_tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + 255) / 256);
+    const bool small = bn == 256 && 4 * pair_tiles <= d.sms / 2;
+    if (small && ov.pair < 1) bn = 128;
     if (ov.bn) bn = ov.bn;
     // A CTA pair (256 x 256 or 256 x 512 tiles, cta_group::2 MMA) when both
     // dimensions exceed one 128-row / 128-column tile and TMA reads the
@@ -258,7 +269,9 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // become 256-wide.
     const Variant *v = nullptr;
     if (producer == 0 && bn >= 256 && M > kBM && N > 128 && ov.pair != 0) {
-        v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
+        // Quads (cta_pair override 2): two pairs of 256 x 256 tiles sharing A.
+        if (ov.pair == 2 && bn == 256) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 2);
+        if (!v) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
         if (!v && bn == 512) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;
     }
@@ -270,8 +283,9 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     pl->v = v;
     bn = v->info.BN;
     const int64_t tile_m = v->info.pair ? 2 * kBM : kBM;
+    const int64_t tile_n = v->info.pair == 2 ? 2 * bn : bn;
     pl->m_tiles = (M + tile_m - 1) / tile_m;
-    pl->tiles = pl->m_tiles * ((N + bn - 1) / bn);
+    pl->tiles = pl->m_tiles * ((N + tile_n - 1) / tile_n);
     // Already refused by the shape check (tile indices are 32-bit).
     if (pl->tiles > INT32_MAX) return GEMMPIPE_ERR_INVALID_VALUE;
     pl->num_kb = (K + kBK - 1) / kBK;
@@ -311,7 +325,7 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
         pl->sk_tiles = slots + T % slots;
         pl->dp_tiles = T - pl->sk_tiles;
     }
-    pl->grid = static_cast<int>(v->info.pair ? 2 * pl->units : pl->units);
+    pl->grid = static_cast<int>(pl->cluster() * pl->units);
     // Tile rows per group ~ sqrt(units): the tiles of a wave then cover
     // about sqrt(units) panels of A and as many of B, the fewest bytes.
     int64_t gm = 1;
@@ -546,7 +560,8 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
         // Boxes: A 64 (k) x 128 rows, B 64 (n) x 64 (k); a pair CTA loads the
         // same boxes for its half -- or, when N is a multiple of 64, each
         // MMA's share of B in one 3-D box of 64-column groups.
-        if (!encode_2d(&ta, A, M, K, lda, kBM)) return GEMMPIPE_ERR_INTERNAL;
+        // A quad's CTA loads half of its 128 rows of a k-block (and multicasts it).
+        if (!encode_2d(&ta, A, M, K, lda, pl.v->info.pair == 2 ? kBM / 2 : kBM)) return GEMMPIPE_ERR_INTERNAL;
         const int per_mma = pl.v->info.BN / (pl.v->info.BN > 256 ? pl.v->info.BN / 256 : 1) / 2 / 64;
         b_groups = pl.v->info.pair && N % 64 == 0 && encode_b_groups(&tb, B, K, N, ldb, kBK, per_mma) ? 1 : 0;
         if (!b_groups && !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
@@ -1218,7 +1233,7 @@ gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, int64_t K, cons
     plan->producer = f.producer;
     plan->BM = f.pair ? 2 * f.BM : f.BM;
     plan->cta_pair = f.pair;
-    plan->BN = f.BN;
+    plan->BN = f.pair == 2 ? 2 * f.BN : f.BN;  // a quad's tile is two pairs' tiles wide
     plan->BK = f.BK;
     plan->stages = f.stages;
     plan->k_chunk = static_cast<int>(pl.kb_per_chunk * f.BK < K ? pl.kb_per_chunk * f.BK : K);
@@ -1240,7 +1255,7 @@ gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, i
     if (producer < -1 || producer > 2) return GEMMPIPE_ERR_INVALID_VALUE;
     if (bn != 0 && bn != 128 && bn != 256 && bn != 512) return GEMMPIPE_ERR_INVALID_VALUE;
     if (stages < 0 || stages > 16) return GEMMPIPE_ERR_INVALID_VALUE;
-    if (cta_pair < -1 || cta_pair > 1) return GEMMPIPE_ERR_INVALID_VALUE;
+    if (cta_pair < -1 || cta_pair > 2) return GEMMPIPE_ERR_INVALID_VALUE;
     if (split < -1 || split > 1) return GEMMPIPE_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_override.producer = producer;

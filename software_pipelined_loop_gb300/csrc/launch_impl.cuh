@@ -47,7 +47,7 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     cfg.numAttrs = 1;
     if constexpr (Cfg::PAIR) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.x = Cfg::CLUSTER;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
@@ -57,8 +57,8 @@ cudaError_t launch_cfg(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     return cudaGetLastError();
 }
 
-// Number of CTA pairs of this variant the current device can hold at once
-// (0 on error or for single-CTA variants).
+// Number of clusters (CTA pairs, or quads of two pairs) of this variant the
+// current device can hold at once (0 on error or for single-CTA variants).
 template <class Cfg>
 int max_pairs_cfg()
 {
@@ -81,12 +81,13 @@ int max_pairs_cfg()
         int sms = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1), 1, 1);
+        constexpr int C = Cfg::CLUSTER;
+        cfg.gridDim = dim3(C * (sms / C > 0 ? sms / C : 1), 1, 1);
         cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = C;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -104,7 +105,7 @@ template <class Cfg>
 constexpr Variant make_variant()
 {
     return Variant{{Cfg::LDG ? 1 : 0, Cfg::INT_OUT ? 1 : 0, Cfg::CONVERT ? 1 : 0, Cfg::BM, Cfg::BN, Cfg::BK,
-                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::PAIR ? 1 : 0, Cfg::THREADS, Cfg::SMEM_BYTES,
+                    Cfg::STAGES, Cfg::I8_STAGES, Cfg::QUAD ? 2 : (Cfg::PAIR ? 1 : 0), Cfg::THREADS, Cfg::SMEM_BYTES,
                     Cfg::SUM_IN_C ? 0 : 1, Cfg::TRACE ? 1 : 0},
                    &launch_cfg<Cfg>, &max_pairs_cfg<Cfg>};
 }

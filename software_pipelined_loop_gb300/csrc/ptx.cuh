@@ -313,6 +313,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// tma_load_2d_pair multicast: the box lands at `dst` in every CTA of
+// `mask`, and each destination's completion is counted on the barrier at
+// this offset in the leader CTA of the destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void *tmap, uint32_t bar_cluster,
+                                                    int32_t x, int32_t y, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
 // 3-D form of tma_load_2d_pair (coordinates x, y, z from the innermost).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap, uint32_t bar_cluster,
                                                  int32_t x, int32_t y, int32_t z)

@@ -15,7 +15,8 @@ struct VariantInfo {
     int convert;   // 1: int8 tiles by TMA, widened to fp16 in shared memory
     int BM, BN, BK, stages;
     int i8_stages;
-    int pair;  // 1: cluster of two CTAs, tcgen05.mma.cta_group::2, 256-row tiles
+    int pair;  // 1: cluster of two CTAs, tcgen05.mma.cta_group::2, 256-row tiles;
+               // 2: a quad (cluster of two such pairs sharing A), 256 x 2BN tiles
     int threads;
     int smem_bytes;
     int split_ok;  // 1: the epilogue can take split (stream-K) tiles

@@ -74,7 +74,7 @@ def test_host_side_argument_checks(lib):
     assert s8(4, 0, 4, None, None, None, None) == gemmpipe.OK
     assert lib.gemmpipe_set_plan_override(3, 0, 0, -1, -1) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 192, 0, -1, -1) == gemmpipe.ERR_INVALID_VALUE
-    assert lib.gemmpipe_set_plan_override(-1, 0, 0, 2, -1) == gemmpipe.ERR_INVALID_VALUE
+    assert lib.gemmpipe_set_plan_override(-1, 0, 0, 3, -1) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 0, 0, -1, 2) == gemmpipe.ERR_INVALID_VALUE
     assert lib.gemmpipe_set_plan_override(-1, 0, 0, -1, -1) == gemmpipe.OK
     assert lib.gemmpipe_test_inject_stall(3, 0) == gemmpipe.ERR_INVALID_VALUE

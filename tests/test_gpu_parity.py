@@ -501,16 +501,21 @@ def test_split_stall_times_out(dev, dtype):
 @pytest.mark.parametrize("M,N,K", [(256, 256, 64), (257, 264, 200), (1000, 776, 1032), (4093, 3000, 136),
                                    (512, 136, 4096), (200, 1024, 64)])
 def test_cta_pair_matches_single_cta(dev, dtype, M, N, K):
-    # Default plan: CTA pairs (cta_group::2, 256-row tiles).  Stages = 4
-    # selects the single-CTA 128 x 256 variant.  Both must match the oracle.
+    # CTA pairs (cta_group::2, 256-row tiles; asked for, since the planner
+    # takes single 128 x 128 tiles for small problems) and the single-CTA
+    # 128 x 256 variant must both match the oracle.
     A, B = inputs.make_operands(dtype, M, N, K, seed=700 + M + N + K)
     want = oracle.gemm_s8s8s32(A, B) if dtype == "s8" else oracle.gemm_f16f32(A, B)
     run = run_s8 if dtype == "s8" else run_f16
     check = (lambda g: np.testing.assert_array_equal(g, want)) if dtype == "s8" else \
         (lambda g: assert_f16_close(g, want))
-    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
-    assert plan["cta_pair"] == 1 and plan["BM"] == 256
-    check(run(A, B, dev))
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, 1)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+        assert plan["cta_pair"] == 1 and plan["BM"] == 256
+        check(run(A, B, dev))
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     gemmpipe.gemmpipe_set_plan_override(-1, 256, 0, 0)
     try:
         plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
@@ -527,12 +532,16 @@ def test_cta_pair_stall_times_out(dev):
     A, B = inputs.make_operands("f16", M, N, K, seed=17)
     Ad, Bd = to_dev(A, dev), to_dev(B, dev)
     C = torch.zeros((M, N), dtype=torch.float32, device=dev)
-    assert gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)["cta_pair"] == 1
-    gemmpipe.gemmpipe_test_inject_stall(2, 200)
-    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
-    gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
-    assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, 1)
+    try:
+        assert gemmpipe.gemmpipe_plan(1, M, N, K, Ad, Bd, C)["cta_pair"] == 1
+        gemmpipe.gemmpipe_test_inject_stall(2, 200)
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+        gemmpipe.gemm_f16f32(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0)
     assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
 
 
@@ -760,3 +769,78 @@ def test_bn512_stall_times_out(dev):
     finally:
         gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
     assert_f16_close(C.cpu().numpy(), oracle.gemm_f16f32(A, B))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("M,N,K,small", [(512, 512, 512, True), (1024, 1024, 1024, True), (300, 2000, 700, True),
+                                         (1280, 1280, 256, False), (2048, 2048, 128, False)])
+def test_small_problems_take_single_cta_tiles(dev, dtype, M, N, K, small):
+    # At most a quarter of the SM pairs' worth of 256 x 256 tiles: single
+    # CTAs on 128 x 128 tiles (more SMs, a quarter of the epilogue each);
+    # larger problems keep the pairs.  Results match the oracle either way.
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    if small:
+        assert plan["cta_pair"] == 0 and plan["BM"] == 128 and plan["BN"] == 128
+    else:
+        assert plan["cta_pair"] == 1 and plan["BM"] == 256
+    A, B = inputs.make_operands(dtype, M, N, K, seed=950 + M + N + K)
+    if dtype == "s8":
+        np.testing.assert_array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+# ------------------------------------------- quads: two CTA pairs sharing A
+
+@pytest.mark.parametrize("split", [-1, 0, 1], ids=["auto", "whole", "split"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 64),        # one tile, one k-block
+                                   (520, 1030, 1000),     # ragged M, N, K
+                                   (300, 300, 4107),      # the second pair's columns mostly past N
+                                   (512, 256, 640),       # the second pair's columns all past N
+                                   (1024, 2048, 2048),    # several tiles per quad
+                                   (2000, 3000, 257)])    # ragged everything, 5 k-blocks
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+def test_quad_tiles(dev, dtype, M, N, K, split):
+    # Quads (cluster of four CTAs): two CTA pairs compute a 256 x 512 tile
+    # over the same 256 rows; each CTA loads half of its A rows of a k-block
+    # and multicasts it to its counterpart in the other pair.
+    A, B = inputs.make_operands(dtype, M, N, K, seed=970 + M + N + K)
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, 2, split)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+        assert plan["cta_pair"] == 2 and plan["BM"] == 256 and plan["BN"] == 512
+        assert plan["grid"] == 4 * plan["units"]
+        if split == 0:
+            assert plan["split_tiles"] == 0
+        got = run_s8(A, B, dev) if dtype == "s8" else run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    if dtype == "s8":
+        np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(got, oracle.gemm_f16f32(A, B), f"quad {M}x{N}x{K} split={split}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+def test_quad_stall_times_out(dev, dtype):
+    import torch
+    M, N, K = 512, 1024, 2048
+    A, B = inputs.make_operands(dtype, M, N, K, seed=977)
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    C = torch.zeros((M, N), dtype=torch.int32 if dtype == "s8" else torch.float32, device=dev)
+    call = gemmpipe.gemm_s8s8s32 if dtype == "s8" else gemmpipe.gemm_f16f32
+    gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, 2, -1)
+    try:
+        assert gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K, Ad, Bd, C)["cta_pair"] == 2
+        gemmpipe.gemmpipe_test_inject_stall(2, 200)
+        call(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.ERR_TIMEOUT
+        call(M, N, K, Ad, Bd, C)
+        assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+    finally:
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    want = oracle.gemm_s8s8s32(A, B) if dtype == "s8" else oracle.gemm_f16f32(A, B)
+    if dtype == "s8":
+        np.testing.assert_array_equal(C.cpu().numpy(), want)
+    else:
+        assert_f16_close(C.cpu().numpy(), want)

@@ -4,8 +4,8 @@ planned up front, or a call path on which a cudaMalloc/cudaFree stall of the
 whole device is not acceptable).  Its fp16 operand copies live in a fixed
 static scratch array instead of a cudaMalloc'd workspace.
 
-Checked here: on calls in a row of different shapes (a CTA-pair plan, a
-single-CTA plan with N <= 128, and K = 0, which must zero C) the result
+Checked here: on calls in a row of different shapes (a CTA-pair plan,
+single-CTA plans, and K = 0, which must zero C) the result
 equals the CPU oracle's and gemm_s8s8s32's bit for bit -- no call depends on
 what the one before left in the shared scratch; once the library's code is
 loaded on the device, a call on a fresh stream leaves the device's free
@@ -46,8 +46,10 @@ def _fits(M, N, K):
 def test_noalloc_matches_oracle_and_allocating_entry_point(lib):
     import torch
     stream = torch.cuda.current_stream().cuda_stream
-    # CTA pairs (M, N > 128), a single CTA per 128 x 128 tile (N <= 128),
-    # then K = 0 and pairs again, all back to back on one stream.
+    # CTA pairs (24 tiles of 256 x 256), a single CTA per 128 x 128 tile
+    # (N <= 128), K = 0, then single CTAs again (a small problem: at most a
+    # quarter of the SM pairs' worth of pair tiles), all back to back on one
+    # stream.
     cases = [(1000, 1500, 2000, 71), (300, 64, 1000, 72), (257, 190, 0, 73), (777, 300, 3001, 74)]
     for M, N, K, seed in cases:
         assert _fits(M, N, K)
