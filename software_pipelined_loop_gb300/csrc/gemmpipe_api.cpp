@@ -268,9 +268,17 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // operands.  512-wide tiles exist for fp16 output only; elsewhere they
     // become 256-wide.
     const Variant *v = nullptr;
+    // Quads (two pairs of 256 x 256 tiles sharing A): asked for (cta_pair
+    // override 2), or by default when C's rows are off 16-byte boundaries.
+    // Such a C is written with 4-byte stores, and there quads measured 3.5-9%
+    // faster (FP16 4093x3001x4107 81.8 vs 86.2 us, 4096x3001x4096 79.8 vs
+    // 82.9, 2000x3001x2000 41.0 vs 44.9, 8191x6001x4096 269.9 vs 274.8; INT8
+    // 4093x3001x4107 87.9 vs 88.8), while on aligned C they gained or lost a
+    // few percent by shape.
+    const bool c_aligned = aligned16(C) && (ldc * 4) % 16 == 0;
+    const bool want_quad = ov.pair == 2 || (ov.pair == -1 && !c_aligned && !convert);
     if (producer == 0 && bn >= 256 && M > kBM && N > 128 && ov.pair != 0) {
-        // Quads (cta_pair override 2): two pairs of 256 x 256 tiles sharing A.
-        if (ov.pair == 2 && bn == 256) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 2);
+        if (want_quad && bn == 256) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 2);
         if (!v) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
         if (!v && bn == 512) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;

@@ -844,3 +844,18 @@ def test_quad_stall_times_out(dev, dtype):
         np.testing.assert_array_equal(C.cpu().numpy(), want)
     else:
         assert_f16_close(C.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("N,quad", [(3001, True), (3004, False), (1030, True), (1032, False)])
+def test_quads_by_default_for_c_rows_off_16_bytes(dev, dtype, N, quad):
+    # C rows off 16-byte boundaries take 4-byte stores; there the planner
+    # takes quads by default, elsewhere CTA pairs.
+    M, K = 1500, 700
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    assert plan["cta_pair"] == (2 if quad else 1)
+    A, B = inputs.make_operands(dtype, M, N, K, seed=990 + N)
+    if dtype == "s8":
+        np.testing.assert_array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
