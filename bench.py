@@ -72,11 +72,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cuh", "gemm_f16.cu", "gemm_s8.cu",
                   "gemmpipe_api.cpp"]
 TRAFFIC = {
-    # (dtype, M, N, K, cta pair, BN): (bytes per launch, sources hash)
-    ("s8", 4096, 4096, 4096, 1, 256): (138_304_000, "8e62c5d61b061468"),
-    ("f16", 4096, 4096, 4096, 1, 256): (138_573_824, "8e62c5d61b061468"),
-    ("f16", 16384, 128, 16384, 0, 128): (544_323_584, "8e62c5d61b061468"),
-    ("f16", 4093, 3001, 4107, 1, 256): (111_441_920, "8e62c5d61b061468"),
+    # (dtype, M, N, K, cta pair, BN, BK): (bytes per launch, sources hash)
+    ("s8", 4096, 4096, 4096, 1, 256, 64): (138_304_000, "8e62c5d61b061468"),
+    ("f16", 4096, 4096, 4096, 1, 256, 64): (138_573_824, "8e62c5d61b061468"),
+    ("f16", 16384, 128, 16384, 0, 128, 64): (544_323_584, "8e62c5d61b061468"),
+    ("f16", 4093, 3001, 4107, 1, 256, 64): (111_441_920, "8e62c5d61b061468"),
 }
 
 
@@ -91,7 +91,7 @@ def kernel_source_hash() -> str:
 
 def measured_traffic(dtype: str, plan: dict, shape: tuple) -> int | None:
     """Captured DRAM traffic of the launch this plan runs on this shape, or None."""
-    t = TRAFFIC.get((dtype, *shape, plan["cta_pair"], plan["BN"]))
+    t = TRAFFIC.get((dtype, *shape, plan["cta_pair"], plan["BN"], plan["BK"]))
     if t is None or t[1] != kernel_source_hash():
         return None
     return t[0]
@@ -645,7 +645,8 @@ ABLATION = [
     ("pair S=3", "f16", SQUARE, 0, 256, 3, 1, -1),
     ("pair S=4", "f16", SQUARE, 0, 256, 4, 1, -1),
     ("pair S=5", "f16", SQUARE, 0, 256, 5, 1, -1),
-    ("pair S=6 (default)", "f16", SQUARE, 0, 256, 6, 1, -1),
+    ("pair S=6", "f16", SQUARE, 0, 256, 6, 1, -1),
+    ("pair, 128 k per stage, S=3 (default)", "f16", SQUARE, 0, 256, 0, 1, -1),
     ("pair S=6, every tile whole (no stream-K)", "f16", SQUARE, 0, 256, 6, 1, 0),
     ("single CTA 128x256 S=4", "f16", SQUARE, 0, 256, 4, 0, -1),
     ("single CTA 128x128 S=6", "f16", SQUARE, 0, 128, 6, 0, -1),

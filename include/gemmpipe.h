@@ -332,6 +332,14 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, int cta_pair,
                                                           int split);
 
+/*
+ * Test hook: k values per pipeline stage for the following calls of this
+ * process that run on CTA pairs (0 automatic, i.e. 64; 64; or 128: 64 KiB
+ * stages, three deep, eight MMAs per stage).  Other plans keep 64.
+ * Returns INVALID_VALUE for other values.
+ */
+GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_bk(int bk);
+
 /* Frees every workspace of the library (operand copies, stream-K partial
  * sums, host-call buffers) and the host calls' streams and events.  Call it
  * with no work of the library in flight. */

@@ -6,6 +6,8 @@ namespace gp {
 static const Variant kF16Variants[] = {
     make_variant<GemmCfg<256, 4, false, false>>(),  // TMA producer, 128x256 tiles
     make_variant<GemmCfg<256, 6, false, false, false, 1, true>>(),  // CTA pair, 256x256 tiles
+    // CTA pair, 256x256 tiles, 128 k per stage (three 64 KiB stages).
+    make_variant<GemmCfg<256, 3, false, false, false, 1, true, 1, 4, false, false, 128>>(),
     // Quad: two CTA pairs (256x512 tile) sharing A by multicast.
     make_variant<GemmCfg<256, 6, false, false, false, 1, true, 1, 4, false, true>>(),
     // CTA pair, 256x512 tiles: two N = 256 MMAs per k-step into one

@@ -53,14 +53,21 @@ namespace gp {
 constexpr int kStatusTimeout = 4;  // GEMMPIPE_ERR_TIMEOUT
 
 template <int BN_, int STAGES_, bool LDG_, bool INT_OUT_, bool CONVERT_ = false, int I8_STAGES_ = 1,
-          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4, bool TRACE_ = false, bool QUAD_ = false>
+          bool PAIR_ = false, int CONV_GROUPS_ = 1, int CONV_WARPS_ = 4, bool TRACE_ = false, bool QUAD_ = false,
+          int BK_ = 64>
 struct GemmCfg {
     // TRACE: a copy of the kernel that stamps the pipelining trace (the
     // test hook gemmpipe_test_trace); the others carry no trace code.
     static constexpr bool TRACE = TRACE_;
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
-    static constexpr int BK = 64;  // 64 fp16 = 128 bytes = one swizzle-atom row
+    // k values per stage: 64 (one 128-byte swizzle-atom row of fp16), or
+    // 128 on CTA pairs: twice the bytes per copy and per barrier round trip.
+    static constexpr int BK = BK_;
+    // A stage holds A as BK / 64 sub-tiles of BM rows x 64 k (each in the
+    // 128-byte swizzle) and B as 64-column atoms of BK rows.
+    static constexpr int A_SUB_BYTES = BM * 128;
+    static constexpr int B_ATOM_BYTES = BK * 128;
     static constexpr int STAGES = STAGES_;
     static constexpr bool LDG = LDG_;
     static constexpr bool INT_OUT = INT_OUT_;
@@ -148,6 +155,7 @@ struct GemmCfg {
     static_assert(BN != 512 || (PAIR && !INT_OUT && !CONVERT),
                   "512-wide tiles: fp16 CTA pairs only (the INT8 epilogue keeps 128 int32 sums per thread)");
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
+    static_assert(BK == 64 || (BK == 128 && PAIR && !QUAD && !LDG && !CONVERT), "BK = 128: CTA pairs only");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
     static_assert(!PAIR || (BN >= 256 && !LDG), "pair variant: TMA producer, 256- or 512-wide tiles");
@@ -722,22 +730,24 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 if (rank == 0) mbar_arrive_expect_tx(fb_local, pair_bytes);
-                if constexpr (Cfg::QUAD)
+                if constexpr (Cfg::QUAD) {
                     tma_load_2d_pair_mc(sa + pair_i * (Cfg::A_BYTES / 2), tA, fb, k0,
                                         m0 + static_cast<int32_t>(pair_i) * (Cfg::BM / 2), a_mask);
-                else
-                    tma_load_2d_pair(sa, tA, fb, k0, m0);
+                } else {
+#pragma unroll
+                    for (int a = 0; a < Cfg::BK / 64; ++a) tma_load_2d_pair(sa + a * Cfg::A_SUB_BYTES, tA, fb, k0 + 64 * a, m0);
+                }
                 if (p.b_groups) {
                     // One 3-D copy per MMA: its NB64_PER_MMA 64-column groups,
                     // 8 KiB apart in shared memory as the 2-D copies place them.
 #pragma unroll
                     for (int u = 0; u < Cfg::N_MMAS; ++u)
-                        tma_load_3d_pair(sa + Cfg::A_BYTES + u * Cfg::NB64_PER_MMA * 8192, tB, fb, 0, k0,
+                        tma_load_3d_pair(sa + Cfg::A_BYTES + u * Cfg::NB64_PER_MMA * Cfg::B_ATOM_BYTES, tB, fb, 0, k0,
                                          (n0 + u * Cfg::MMA_N) / 64);
                 } else {
 #pragma unroll
                     for (int j = 0; j < Cfg::NB64; ++j)
-                        tma_load_2d_pair(sa + Cfg::A_BYTES + j * 8192, tB, fb,
+                        tma_load_2d_pair(sa + Cfg::A_BYTES + j * Cfg::B_ATOM_BYTES, tB, fb,
                                          n0 + (j / Cfg::NB64_PER_MMA) * Cfg::MMA_N + 64 * (j % Cfg::NB64_PER_MMA),
                                          k0);
                 }
@@ -789,10 +799,10 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
     const uint16_t BOTH = static_cast<uint16_t>(3u << crank);              // this pair's two CTAs
     const uint16_t STAGE_MASK = Cfg::QUAD ? static_cast<uint16_t>(0xF) : BOTH;  // whoever writes the stages
     // Byte offset of the B columns of MMA u of a k-step within a stage's B.
-    constexpr int B_MMA_BYTES = Cfg::NB64_PER_MMA * 8192;
+    constexpr int B_MMA_BYTES = Cfg::NB64_PER_MMA * Cfg::B_ATOM_BYTES;
     // Per-stage, per-k-step descriptors are offsets of these two (see mma_issuer).
     const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);
-    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, 8192, 1024);
+    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, Cfg::B_ATOM_BYTES, 1024);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
@@ -827,7 +837,8 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
                 for (int kk = 0; kk < Cfg::BK / 16; ++kk)
 #pragma unroll
                     for (int u = 0; u < Cfg::N_MMAS; ++u)
-                        umma_f16_pair(d + u * Cfg::MMA_N, dA0 + so + (kk * 32 >> 4),
+                        umma_f16_pair(d + u * Cfg::MMA_N,
+                                      dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
                                       dB0 + so + ((u * B_MMA_BYTES + kk * 2048) >> 4), idesc,
                                       (kb > kc || kk > 0) ? 1u : 0u);
                 issued = true;

@@ -118,6 +118,7 @@ gemmpipe_status_t check_device_pointers(int64_t K, const void *A, const void *B,
 
 struct Override {
     int producer = -1, bn = 0, stages = 0, pair = -1, split = -1;
+    int bk = 0;  // k values per stage: 0 automatic (64), or 64 / 128
 };
 Override g_override;
 
@@ -180,14 +181,14 @@ int64_t Plan::split_bytes() const
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-const Variant *find_variant(int int_out, int convert, int producer, int bn, int stages, int pair)
+const Variant *find_variant(int int_out, int convert, int producer, int bn, int stages, int pair, int bk = 64)
 {
     const Variant *tab = nullptr;
     const int n = int_out ? gp::variants_s8(&tab) : gp::variants_f16(&tab);
     for (int i = 0; i < n; ++i) {
         const gp::VariantInfo &f = tab[i].info;
         if (f.producer == producer && f.convert == convert && f.BN == bn && f.pair == pair && !f.traced &&
-            (stages == 0 || f.stages == stages))
+            f.BK == bk && (stages == 0 || f.stages == stages))
             return &tab[i];
     }
     return nullptr;
@@ -279,6 +280,12 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     const bool want_quad = ov.pair == 2 || (ov.pair == -1 && !c_aligned && !convert);
     if (producer == 0 && bn >= 256 && M > kBM && N > 128 && ov.pair != 0) {
         if (want_quad && bn == 256) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 2);
+        // CTA pairs take 128 k per stage unless a ring depth or 64 k is asked
+        // for (A/B in one process, kernel time: INT8 4096^3 86.4 vs 87.9 us,
+        // FP16 4096^3 87.1 vs 87.7, INT8 1024 x 4096^2 31.5 vs 32.8, FP16
+        // 3072^3 42.5 vs 43.3; ragged FP16 and INT8 8192^3 within +1.2%).
+        const bool bk128 = ov.bk == 128 || (ov.bk == 0 && ov.stages == 0);
+        if (!v && bk128) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1, 128);
         if (!v) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
         if (!v && bn == 512) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);
         if (v && v->max_pairs() < 1) v = nullptr;
@@ -296,8 +303,9 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     pl->tiles = pl->m_tiles * ((N + tile_n - 1) / tile_n);
     // Already refused by the shape check (tile indices are 32-bit).
     if (pl->tiles > INT32_MAX) return GEMMPIPE_ERR_INVALID_VALUE;
-    pl->num_kb = (K + kBK - 1) / kBK;
-    pl->kb_per_chunk = int_out ? kInt8ChunkK / kBK : pl->num_kb;
+    const int bk = v->info.BK;
+    pl->num_kb = (K + bk - 1) / bk;
+    pl->kb_per_chunk = int_out ? kInt8ChunkK / bk : pl->num_kb;
     // Persistent grid: at most one CTA (or CTA pair) per SM (pair) slot.
     // Whole tiles go round-robin; when they leave a partial last wave that
     // is at most 4/5 full, that wave and the one before it are spread over
@@ -571,8 +579,9 @@ gemmpipe_status_t run_plan(Plan pl, int dev, int64_t M, int64_t N, int64_t K, co
         // A quad's CTA loads half of its 128 rows of a k-block (and multicasts it).
         if (!encode_2d(&ta, A, M, K, lda, pl.v->info.pair == 2 ? kBM / 2 : kBM)) return GEMMPIPE_ERR_INTERNAL;
         const int per_mma = pl.v->info.BN / (pl.v->info.BN > 256 ? pl.v->info.BN / 256 : 1) / 2 / 64;
-        b_groups = pl.v->info.pair && N % 64 == 0 && encode_b_groups(&tb, B, K, N, ldb, kBK, per_mma) ? 1 : 0;
-        if (!b_groups && !encode_2d(&tb, B, K, N, ldb, kBK)) return GEMMPIPE_ERR_INTERNAL;
+        const int bk = pl.v->info.BK;
+        b_groups = pl.v->info.pair && N % 64 == 0 && encode_b_groups(&tb, B, K, N, ldb, bk, per_mma) ? 1 : 0;
+        if (!b_groups && !encode_2d(&tb, B, K, N, ldb, bk)) return GEMMPIPE_ERR_INTERNAL;
     }
     CUtensorMap tc;
     std::memset(&tc, 0, sizeof(tc));
@@ -701,7 +710,9 @@ gemmpipe_status_t s8_with_fixed_scratch(int64_t M, int64_t N, int64_t K, const i
     CUtensorMap ta, tb;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
-    if (!encode_2d(&ta, A16, M, K, Kp, kBM) || !encode_2d(&tb, B16, K, N, Np, kBK)) return GEMMPIPE_ERR_INTERNAL;
+    if (!encode_2d(&ta, A16, M, K, Kp, pl.v->info.pair == 2 ? kBM / 2 : kBM) ||
+        !encode_2d(&tb, B16, K, N, Np, pl.v->info.BK))
+        return GEMMPIPE_ERR_INTERNAL;
     GemmParams p;
     p.M = M;
     p.N = N;
@@ -1271,6 +1282,14 @@ gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, int stages, i
     g_override.stages = stages;
     g_override.pair = cta_pair;
     g_override.split = split;
+    return GEMMPIPE_OK;
+}
+
+gemmpipe_status_t gemmpipe_set_plan_bk(int bk)
+{
+    if (bk != 0 && bk != 64 && bk != 128) return GEMMPIPE_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_override.bk = bk;
     return GEMMPIPE_OK;
 }
 

@@ -66,6 +66,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gemmpipe_stage_smem_bytes": (_i64, [_int, _int, _int, _int, _int]),
         "gemmpipe_plan": (_int, [_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.POINTER(PlanT)]),
         "gemmpipe_set_plan_override": (_int, [_int, _int, _int, _int, _int]),
+        "gemmpipe_set_plan_bk": (_int, [_int]),
         "gemmpipe_release_workspaces": (_int, []),
         "gemmpipe_timing_enable": (_int, [_int]),
         "gemmpipe_timing_read": (_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64),
@@ -177,6 +178,10 @@ def gemmpipe_plan(dtype: int, M, N, K, A=None, B=None, C=None) -> dict:
 def gemmpipe_set_plan_override(producer: int = -1, bn: int = 0, stages: int = 0, cta_pair: int = -1,
                                split: int = -1) -> None:
     _check(load().gemmpipe_set_plan_override(producer, bn, stages, cta_pair, split), "gemmpipe_set_plan_override")
+
+
+def gemmpipe_set_plan_bk(bk: int) -> None:
+    _check(load().gemmpipe_set_plan_bk(bk), "gemmpipe_set_plan_bk")
 
 
 def gemmpipe_release_workspaces() -> None:

@@ -859,3 +859,48 @@ def test_quads_by_default_for_c_rows_off_16_bytes(dev, dtype, N, quad):
         np.testing.assert_array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
     else:
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
+# ----------------------------------------------- 128 k per stage (CTA pairs)
+
+@pytest.mark.parametrize("split", [-1, 0, 1], ids=["auto", "whole", "split"])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (520, 1030, 1000), (300, 600, 4107), (1024, 2048, 4160),
+                                   (2000, 3000, 257), (777, 512, 64)])
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+def test_bk128_pair_tiles(dev, dtype, M, N, K, split):
+    # Stages of 128 k (A as two 64-k sub-tiles, B as 64-column atoms of 128
+    # rows), three deep; ragged K tails, one k-block, INT8 chunks of eight
+    # k-blocks.
+    A, B = inputs.make_operands(dtype, M, N, K, seed=1010 + M + N + K)
+    gemmpipe.gemmpipe_set_plan_override(-1, 256, 0, 1, split)
+    gemmpipe.gemmpipe_set_plan_bk(128)
+    try:
+        plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+        assert plan["BK"] == 128 and plan["stages"] == 3 and plan["cta_pair"] == 1
+        assert plan["k_blocks"] == (K + 127) // 128
+        got = run_s8(A, B, dev) if dtype == "s8" else run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_bk(0)
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    if dtype == "s8":
+        np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(got, oracle.gemm_f16f32(A, B), f"bk128 {M}x{N}x{K} split={split}")
+
+
+def test_bk128_int8_chunk_extremes(dev):
+    # Partial sums of 1024 k just below 2^24 with odd values: exact only if
+    # every accumulation chunk stays within 1024 k (eight 128-k blocks).
+    M, N, K = 300, 520, 4096
+    rng = np.random.default_rng(23)
+    A = np.where(rng.random((M, K)) < 0.97, -128, 127).astype(np.int8)
+    B = np.where(rng.random((K, N)) < 0.97, -128, 127).astype(np.int8)
+    gemmpipe.gemmpipe_set_plan_override(-1, 256, 0, 1, -1)
+    gemmpipe.gemmpipe_set_plan_bk(128)
+    try:
+        assert gemmpipe.gemmpipe_plan(0, M, N, K)["BK"] == 128
+        got = run_s8(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_bk(0)
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    np.testing.assert_array_equal(got, oracle.gemm_s8s8s32(A, B))
