@@ -73,10 +73,10 @@ KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cu
                   "gemmpipe_api.cpp"]
 TRAFFIC = {
     # (dtype, M, N, K, cta pair, BN, BK): (bytes per launch, sources hash)
-    ("s8", 4096, 4096, 4096, 1, 256, 64): (138_304_000, "8e62c5d61b061468"),
-    ("f16", 4096, 4096, 4096, 1, 256, 64): (138_573_824, "8e62c5d61b061468"),
-    ("f16", 16384, 128, 16384, 0, 128, 64): (544_323_584, "8e62c5d61b061468"),
-    ("f16", 4093, 3001, 4107, 1, 256, 64): (111_441_920, "8e62c5d61b061468"),
+    ("s8", 4096, 4096, 4096, 1, 256, 128): (140_375_040, "9b4e8d2aab1f547a"),
+    ("f16", 4096, 4096, 4096, 1, 256, 128): (141_610_752, "9b4e8d2aab1f547a"),
+    ("f16", 16384, 128, 16384, 0, 128, 64): (544_113_664, "9b4e8d2aab1f547a"),
+    ("f16", 4093, 3001, 4107, 2, 512, 64): (85_971_968, "9b4e8d2aab1f547a"),
 }
 
 
@@ -610,7 +610,8 @@ def run_gpu(args) -> int:
         "parity": parity or None,
         "kernel_ms": head["kernel_ms"], "aux_ms": head["aux_ms"],
         "plan": {k: head["plan"][k] for k in ("producer", "BM", "BN", "BK", "stages", "threads", "cta_pair", "grid",
-                                              "units", "tiles", "split_tiles", "k_blocks", "operand_copy")},
+                                              "units", "tiles", "split_tiles", "k_blocks", "operand_copy",
+                                              "smem_bytes")},
         "copy_ref_gbs": round(copy_ref["gbs"], 1),
         "int8_step_floor": int8_floor,
         "library_context": context,

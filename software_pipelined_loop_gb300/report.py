@@ -125,17 +125,22 @@ def compute_load(L: Launch) -> dict:
     BM, BN, BK = int(L.plan["BM"]), int(L.plan["BN"]), int(L.plan["BK"])
     elem = 2  # the tensor cores read fp16 (INT8 operands are widened)
     flop_per_byte = 2.0 * BM * BN * BK / ((BM * BK + BK * BN) * elem)
-    pair = bool(L.plan.get("cta_pair"))
-    # One MMA instruction covers the whole tile for K = 16 (cta_group::2
-    # for a pair: one instruction for both CTAs).
-    mma = BK // 16
-    # Copy instructions: TMA boxes of A (one, 128 rows, per CTA) and of B
-    # (64-column boxes of the CTA's columns); the bounded-load producer
-    # issues 16-byte loads instead.
-    ctas = 2 if pair else 1
+    # CTAs per tile: 1 (single CTA), 2 (CTA pair), 4 (quad: two pairs).
+    ctas = {0: 1, 1: 2, 2: 4}[int(L.plan.get("cta_pair", 0))]
+    pairs = max(1, ctas // 2)
+    # One MMA instruction covers a pair's (or a single CTA's) tile columns
+    # up to N = 256 for K = 16 (cta_group::2 for a pair: one instruction for
+    # both CTAs); a quad's two pairs issue their own.
+    mma = pairs * (BK // 16) * max(1, BN // pairs // 256)
+    # Copy instructions per CTA: A as 64-k boxes (a quad's CTA loads half of
+    # its rows and multicasts them), B as 64-column boxes of BK rows, or one
+    # 3-D box per MMA when N is a multiple of 64 on pairs; the bounded-load
+    # producer issues 16-byte loads instead.
     cta_bn = BN // ctas
     if int(L.plan.get("producer", 0)) == 0:
-        copies = ctas * (1 + cta_bn // 64)
+        a_boxes = BK // 64
+        b_boxes = max(1, BN // pairs // 256) if ctas > 1 and L.N % 64 == 0 else cta_bn // 64
+        copies = ctas * (a_boxes + b_boxes)
         copy_unit = "TMA box"
     else:
         copies = ctas * ((128 * BK + BK * cta_bn) * elem // 16)
@@ -340,10 +345,14 @@ def launch_from_bench(line: dict, workload: str | None, peaks: tuple[float, floa
     if workload is None or workload == line["config"]["workload"]:
         cfg = line["config"]
         name, dtype, M, N, K = cfg["workload"], line["dtype"], cfg["M"], cfg["N"], cfg["K"]
-        plan, kms, step = cfg["plan"], line["kernel_ms"], line["ms_per_step"]
+        plan = line["plan"] if "plan" in line else cfg["plan"]
+        kms, step = line["kernel_ms"], line["ms_per_step"]
         traffic = line["roofline"].get("traffic")
     else:
         sec = line["secondary"][workload]
+        if "plan" not in sec:
+            raise SystemExit(f"the bench line's entry for {workload} carries no plan: run "
+                             f"bench.py --shape <dtype>,M,N,K for that shape and report its headline")
         name, dtype = workload, sec.get("dtype", "f16")
         M, N, K = sec["shape"]
         plan, kms, step = sec["plan"], sec["kernel_ms"], sec["ms_per_step"]

@@ -61,8 +61,17 @@ def test_compute_load_ratios():
     c = report.compute_load(launch())
     assert c["flop_per_byte"] == pytest.approx(128.0)
     # Pair: 4 tcgen05.mma (K = 16) per 64-deep k-block against 2 x (1 A box +
-    # 2 B boxes) TMA copies: 0.67:1, low -> asynchronous loads pay.
-    assert (c["mma_per_kblock"], c["copies_per_kblock"]) == (4, 6) and c["class"] == "low"
+    # one 3-D B box) TMA copies: 1:1, low -> asynchronous loads pay.
+    assert (c["mma_per_kblock"], c["copies_per_kblock"]) == (4, 4) and c["class"] == "low"
+    # N not a multiple of 64: B as two 64-column 2-D boxes per CTA.
+    r = report.compute_load(launch(shape=(4093, 3001, 4107)))
+    assert r["copies_per_kblock"] == 6
+    # 128 k per stage: 8 MMAs against 2 x (2 A boxes + one 3-D B box).
+    b = report.compute_load(launch(plan=dict(PAIR_PLAN, BK=128, stages=3)))
+    assert (b["mma_per_kblock"], b["copies_per_kblock"]) == (8, 6)
+    # Quad (256 x 512 tile): each pair issues its 4 MMAs; 4 CTAs x (1 A box + 1 B box).
+    q = report.compute_load(launch(plan=dict(PAIR_PLAN, BN=512, cta_pair=2)))
+    assert (q["mma_per_kblock"], q["copies_per_kblock"]) == (8, 8)
     s = report.compute_load(launch(plan=SKINNY_PLAN))
     assert s["flop_per_byte"] == pytest.approx(64.0) and s["copies_per_kblock"] == 3
     ldg = report.compute_load(launch(plan=dict(SKINNY_PLAN, producer=1)))
@@ -102,8 +111,8 @@ def test_parse_raw_csv_and_bench_line(tmp_path):
     c = report.parse_ncu_raw_csv(csv_text)
     assert c["launch__registers_per_thread"] == "168" and c["dram__bytes_read.sum"] == "85.6"
     assert c["__units__"]["dram__bytes_read.sum"] == "Mbyte"
-    line = {"dtype": "s8", "kernel_ms": 0.0907, "ms_per_step": 0.1027,
-            "config": {"workload": "int8_4096", "M": 4096, "N": 4096, "K": 4096, "plan": PAIR_PLAN},
+    line = {"dtype": "s8", "kernel_ms": 0.0907, "ms_per_step": 0.1027, "plan": PAIR_PLAN,
+            "config": {"workload": "int8_4096", "M": 4096, "N": 4096, "K": 4096},
             "roofline": {"traffic": None},
             "secondary": {"fp16_skinny": {"shape": [16384, 128, 16384], "dtype": "f16", "plan": SKINNY_PLAN,
                                           "kernel_ms": 0.1027, "ms_per_step": 0.1023, "roofline": {}}}}
@@ -111,6 +120,10 @@ def test_parse_raw_csv_and_bench_line(tmp_path):
     assert (L.name, L.dtype, L.M, L.step_ms) == ("int8_4096", "s8", 4096, 0.1027)
     S = report.launch_from_bench(line, "fp16_skinny", (1917.5, 6785.2, "measured"))
     assert (S.N, S.plan["BN"]) == (128, 128)
+    # Secondary entries of the compact line carry no plan: refused with a hint.
+    line["secondary"]["fp16_1024"] = {"value": 150.0, "unit": "TFLOPS", "ms": 0.014}
+    with pytest.raises(SystemExit, match="--shape"):
+        report.launch_from_bench(line, "fp16_1024", (1917.5, 6785.2, "measured"))
     p = tmp_path / "b.json"
     p.write_text("noise\n" + json.dumps(line) + "\n")
     q = tmp_path / "raw.csv"
