@@ -152,6 +152,48 @@ def test_misaligned_base_pointers(dev):
         assert cb[0].item() == 0 and cb[M * N + 1:].abs().sum().item() == 0
 
 
+@pytest.mark.parametrize("dtype,M,N,K", [("f16", 600, 1000, 512), ("f16", 517, 771, 300),
+                                         ("s8", 600, 1000, 1100), ("s8", 300, 517, 200)])
+@pytest.mark.parametrize("c_off", [4, 8, 12])
+def test_c_rows_off_16_bytes(dev, dtype, M, N, K, c_off):
+    """C rows that do not start on 16-byte boundaries (C's base 4, 8 or 12
+    bytes past one; N a multiple of 8 or odd, so that the rows' offsets vary)
+    on every tile plan, split tiles included: no TMA store can take them, so
+    the epilogue writes one row piece per warp store.  Every element against
+    the oracle, and nothing written outside C."""
+    import torch
+    A, B = inputs.make_operands(dtype, M, N, K, seed=71 + c_off)
+    ref = oracle.gemm_s8s8s32(A, B) if dtype == "s8" else oracle.gemm_f16f32(A, B)
+    pad = 64
+    cdt = torch.int32 if dtype == "s8" else torch.float32
+    buf = torch.full((pad + M * N + pad,), 777, dtype=cdt, device=dev)
+    c_ptr = buf.data_ptr() + 4 * pad + c_off
+    assert c_ptr % 16 == c_off
+    Ad, Bd = to_dev(A, dev), to_dev(B, dev)
+    fn = gemmpipe.gemm_s8s8s32 if dtype == "s8" else gemmpipe.gemm_f16f32
+    # (producer, bn, stages, cta_pair, split): default, CTA pair, quad, single CTA, pair with forced split
+    plans = [(-1, 0, 0, -1, -1), (-1, 256, 0, 1, -1), (-1, 256, 0, 2, -1), (-1, 128, 0, 0, -1), (-1, 256, 0, 1, 1)]
+    for ov in plans:
+        gemmpipe.gemmpipe_set_plan_override(*ov)
+        try:
+            plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K, Ad, Bd, c_ptr)
+            assert plan["vector_store"] == 0
+            buf.fill_(777)
+            fn(M, N, K, Ad, Bd, c_ptr)
+            assert gemmpipe.gemmpipe_get_device_status() == gemmpipe.OK
+        finally:
+            gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+        host = buf.cpu().numpy()
+        c0 = pad + c_off // 4
+        got = host[c0:c0 + M * N].reshape(M, N)
+        assert (host[:c0] == 777).all(), (ov, "elements before C written")
+        assert (host[c0 + M * N:] == 777).all(), (ov, "elements after C written")
+        if dtype == "s8":
+            assert np.array_equal(got, ref), (ov, plan)
+        else:
+            assert_f16_close(got, ref, str((ov, plan["cta_pair"], plan["BN"])))
+
+
 def test_guard_bands_untouched(dev):
     import torch
     M, N, K = 257, 264, 128
