@@ -315,6 +315,11 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // cuts a unit's k-blocks to a third or less.  Measured on GB300: a
     // split costs its fix-up and, with every SM streaming operands at once,
     // a slower k-loop, so it pays only when the work per unit drops a lot.
+    // Quads (the plan for C rows off 16-byte boundaries, whose row-piece
+    // stores make every item's epilogue long) split only a last wave at
+    // most half full after two or more full waves (measured: 96 tiles on 36
+    // quads 82.3 vs 79.6 us split vs whole, 48 tiles 40.9 vs 39.7, 384
+    // tiles 271 vs 267; 120 tiles 92.9 vs 99.1).
     const int64_t slots = v->info.pair ? v->max_pairs() : d.sms;
     const int64_t T = pl->tiles;
     const bool split = split_ok && v->info.split_ok && ov.split != 0;
@@ -337,7 +342,8 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
             pl->sk_tiles = T;
         }
     } else if (split && T > slots && T % slots != 0 && pl->num_kb > 1 &&
-               (ov.split == 1 || 5 * (T % slots) <= 4 * slots)) {
+               (ov.split == 1 || (v->info.pair == 2 ? (2 * (T % slots) <= slots && T >= 2 * slots)
+                                                    : 5 * (T % slots) <= 4 * slots))) {
         pl->sk_tiles = slots + T % slots;
         pl->dp_tiles = T - pl->sk_tiles;
     }

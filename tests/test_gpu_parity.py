@@ -903,6 +903,16 @@ def test_quads_by_default_for_c_rows_off_16_bytes(dev, dtype, N, quad):
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
 
 
+def test_quad_split_rule(dev):
+    # Quads split only a last wave at most half full after two full waves.
+    for M, N, K in ((4093, 3001, 4107), (2000, 3001, 2000), (3000, 5001, 4000), (8191, 6001, 4096)):
+        p = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert p["cta_pair"] == 2
+        T, G = p["tiles"], p["units"]
+        want = G + T % G if (T > G and T % G and 2 * (T % G) <= G and T >= 2 * G) else 0
+        assert p["split_tiles"] == want, (M, N, K, p)
+
+
 # ----------------------------------------------- 128 k per stage (CTA pairs)
 
 @pytest.mark.parametrize("split", [-1, 0, 1], ids=["auto", "whole", "split"])

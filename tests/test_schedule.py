@@ -21,7 +21,8 @@ tiles over u = min(slots, ceil(tiles * k_blocks / 8)) units when u is at
 least three times the tile count (unless the GEMM is memory-bound and its
 tiles already fill half the slots); more tiles than slots with a partial
 last wave at most 4/5 full split the last two waves' tiles (slots + tiles %
-slots) over all slots.  `force` is the plan override that splits wherever
+slots) over all slots -- for quads (the plan for C rows off 16-byte
+boundaries) only a last wave at most half full after two full waves.  `force` is the plan override that splits wherever
 the schedule can.
 """
 from __future__ import annotations
@@ -33,13 +34,16 @@ import pytest
 MIN_SPLIT_KB = 8
 
 
-def plan(tiles: int, slots: int, num_kb: int, memory_bound: bool = False, force: bool = False):
+def plan(tiles: int, slots: int, num_kb: int, memory_bound: bool = False, force: bool = False,
+         quad: bool = False):
     units, dp_tiles, sk_tiles = min(tiles, slots), tiles, 0
+    tail = tiles % slots
+    tail_rule = (2 * tail <= slots and tiles >= 2 * slots) if quad else 5 * tail <= 4 * slots
     if tiles < slots:
         u = min(slots, -(-tiles * num_kb // MIN_SPLIT_KB))
         if u > tiles and (force or (u >= 3 * tiles and not (memory_bound and 2 * tiles >= slots))):
             units, dp_tiles, sk_tiles = u, 0, tiles
-    elif tiles > slots and tiles % slots and num_kb > 1 and (force or 5 * (tiles % slots) <= 4 * slots):
+    elif tiles > slots and tail and num_kb > 1 and (force or tail_rule):
         sk_tiles = slots + tiles % slots
         dp_tiles = tiles - sk_tiles
     return units, dp_tiles, sk_tiles
@@ -180,3 +184,15 @@ def test_grouped_tile_order_is_a_bijection(m_tiles, n_tiles, units):
         # A wave of 76 tiles touches 8 rows of A panels and 10 columns of B.
         wave = {tile_coords(t, m_tiles, n_tiles, gm) for t in range(76)}
         assert len({m for m, _ in wave}) == 8 and len({n for _, n in wave}) == 10
+
+
+def test_quad_split_rule_matches_the_measured_cases():
+    # 36 quads: split only a last wave at most half full after >= 2 waves.
+    assert plan(96, 36, 65, quad=True)[2] == 0      # 2.67 waves: whole tiles measured faster
+    assert plan(48, 36, 32, quad=True)[2] == 0      # 1.33 waves: whole
+    assert plan(384, 36, 64, quad=True)[2] == 0     # 10.67 waves: whole
+    assert plan(120, 36, 63, quad=True)[2] == 36 + 120 % 36  # 3.33 waves: split measured 6% faster
+    # Pairs keep the 4/5 rule.
+    assert plan(96, 36, 65)[2] == 36 + 96 % 36
+    # Forced splits ignore both rules; the schedule invariants hold either way.
+    assert plan(96, 36, 65, quad=True, force=True)[2] == 36 + 96 % 36
