@@ -334,9 +334,11 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, 
 
 /*
  * Test hook: k values per pipeline stage for the following calls of this
- * process that run on CTA pairs (0 automatic, i.e. 64; 64; or 128: 64 KiB
- * stages, three deep, eight MMAs per stage).  Other plans keep 64.
- * Returns INVALID_VALUE for other values.
+ * process (0 automatic: 128 on CTA pairs and on fp16 single-CTA plans with
+ * N <= 128, unless a ring depth is forced, 64 elsewhere; 64; or 128: 64 KiB
+ * stages, three deep -- on CTA pairs, and on single CTAs with 128 x 128
+ * fp16 tiles).  Plans without a 128-k variant
+ * keep 64.  Returns INVALID_VALUE for other values.
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_bk(int bk);
 

@@ -22,6 +22,9 @@ static const Variant kF16Variants[] = {
     make_variant<GemmCfg<256, 4, false, false, false, 1, true>>(),
     make_variant<GemmCfg<256, 5, false, false, false, 1, true>>(),
     make_variant<GemmCfg<128, 6, false, false>>(),  // TMA producer, 128x128 tiles (N <= 128)
+    // The same tiles with 128 k per stage (three 64 KiB stages): each A row
+    // is read 256 bytes at a time (plan override bk = 128).
+    make_variant<GemmCfg<128, 3, false, false, false, 1, false, 1, 4, false, false, 128>>(),
     make_variant<GemmCfg<256, 4, true, false>>(),   // bounded-load producer (misaligned inputs)
     make_variant<GemmCfg<128, 6, true, false>>(),
     // Copies of the pair kernels at 6 and 1 stages that stamp the

@@ -155,7 +155,7 @@ struct GemmCfg {
     static_assert(BN != 512 || (PAIR && !INT_OUT && !CONVERT),
                   "512-wide tiles: fp16 CTA pairs only (the INT8 epilogue keeps 128 int32 sums per thread)");
     static_assert(STAGES >= 1 && STAGES <= 16, "ring depth");
-    static_assert(BK == 64 || (BK == 128 && PAIR && !QUAD && !LDG && !CONVERT), "BK = 128: CTA pairs only");
+    static_assert(BK == 64 || (BK == 128 && !QUAD && !LDG && !CONVERT), "BK = 128: TMA producer, no quads");
     static_assert(!(LDG && INT_OUT), "INT8 operands are widened into an aligned workspace");
     static_assert(!CONVERT || (INT_OUT && !LDG && I8_STAGES >= 1), "converter variant is INT8 with TMA");
     static_assert(!PAIR || (BN >= 256 && !LDG), "pair variant: TMA producer, 256- or 512-wide tiles");
@@ -530,9 +530,11 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
                 mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                tma_load_2d(sa, tA, fb, k0, m0);
 #pragma unroll
-                for (int j = 0; j < Cfg::NB64; ++j) tma_load_2d(sa + Cfg::A_BYTES + j * 8192, tB, fb, n0 + 64 * j, k0);
+                for (int a = 0; a < Cfg::BK / 64; ++a) tma_load_2d(sa + a * Cfg::A_SUB_BYTES, tA, fb, k0 + 64 * a, m0);
+#pragma unroll
+                for (int j = 0; j < Cfg::NB64; ++j)
+                    tma_load_2d(sa + Cfg::A_BYTES + j * Cfg::B_ATOM_BYTES, tB, fb, n0 + 64 * j, k0);
                 if constexpr (Cfg::TRACE) {
                     if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
                 }
@@ -884,7 +886,7 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
     // the start-address field (address >> 4, bits [0,14)); shared memory
     // stays under 256 KB so the sum never carries out of that field.
     const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);
-    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, 8192, 1024);
+    const uint64_t dB0 = umma_desc_sw128(sbase + Cfg::A_BYTES, Cfg::B_ATOM_BYTES, 1024);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc = 0, acc_phase = 0;
@@ -916,9 +918,12 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
                 tc_fence_after_sync();
                 const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
                 umma_f16(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
+                // k-step kk: A sub-tile kk / 4 (64 k each), 32 bytes per
+                // 16 k within it; B 16 rows of its atoms per 16 k.
 #pragma unroll
                 for (int kk = 1; kk < Cfg::BK / 16; ++kk)
-                    umma_f16(d, dA0 + so + (kk * 32 >> 4), dB0 + so + (kk * 2048 >> 4), idesc, 1u);
+                    umma_f16(d, dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
+                             dB0 + so + (kk * 2048 >> 4), idesc, 1u);
                 issued = true;
                 umma_commit(smem_u32(&ctl->empty[stage]));
                 if (++stage == Cfg::STAGES) {

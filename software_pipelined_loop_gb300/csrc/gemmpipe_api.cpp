@@ -202,7 +202,8 @@ const Variant *traced_twin(const Variant *v)
     for (int i = 0; i < n; ++i) {
         const gp::VariantInfo &f = tab[i].info;
         if (f.traced && f.producer == v->info.producer && f.convert == v->info.convert && f.BN == v->info.BN &&
-            f.pair == v->info.pair && f.stages == v->info.stages && f.int_out == v->info.int_out)
+            f.pair == v->info.pair && f.stages == v->info.stages && f.int_out == v->info.int_out &&
+            f.BK == v->info.BK)
             return &tab[i];
     }
     return nullptr;
@@ -291,6 +292,13 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
         if (v && v->max_pairs() < 1) v = nullptr;
     }
     if (bn == 512 && (!v || !v->info.pair)) bn = 256;
+    // Single CTAs take 128 k per stage when asked for (plan override), and
+    // by default for fp16 with N <= 128 (the skinny, memory-bound case: each
+    // A row is read 256 bytes at a time; A/B in one process, kernel time:
+    // 16384 x 128 x 16384 112.1 vs 113.7 us, 16384 x 64 x 16384 111.5 vs
+    // 112.6, 8192 x 128 x 8192 and 32768 x 128 x 8192 within 0.3%).
+    const bool single_bk128 = ov.bk == 128 || (ov.bk == 0 && ov.stages == 0 && !int_out && N <= 128);
+    if (!v && single_bk128 && producer == 0 && !convert) v = find_variant(int_out, 0, 0, bn, ov.stages, 0, 128);
     if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, ov.stages, 0);
     if (!v) v = find_variant(int_out, convert ? 1 : 0, producer, bn, 0, 0);
     if (!v) return GEMMPIPE_ERR_INTERNAL;

@@ -903,6 +903,24 @@ def test_quads_by_default_for_c_rows_off_16_bytes(dev, dtype, N, quad):
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (1000, 128, 4107), (16384, 128, 2048), (300, 100, 129),
+                                   (520, 64, 1000)])
+def test_bk128_single_cta_tiles(dev, M, N, K):
+    # Single CTAs on 128 x 128 tiles with 128 k per stage (A as two 64-k
+    # sub-tiles per stage): one k-block, ragged K tails, N below 128.
+    A, B = inputs.make_operands("f16", M, N, K, seed=1100 + M + N + K)
+    gemmpipe.gemmpipe_set_plan_override(-1, 128, 0, 0, -1)
+    gemmpipe.gemmpipe_set_plan_bk(128)
+    try:
+        plan = gemmpipe.gemmpipe_plan(1, M, N, K)
+        assert plan["BK"] == 128 and plan["stages"] == 3 and plan["cta_pair"] == 0 and plan["BN"] == 128
+        got = run_f16(A, B, dev)
+    finally:
+        gemmpipe.gemmpipe_set_plan_bk(0)
+        gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+    assert_f16_close(got, oracle.gemm_f16f32(A, B), f"{M}x{N}x{K}")
+
+
 def test_quad_split_rule(dev):
     # Quads split only a last wave at most half full after two full waves.
     for M, N, K in ((4093, 3001, 4107), (2000, 3001, 2000), (3000, 5001, 4000), (8191, 6001, 4096)):
