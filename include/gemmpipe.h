@@ -325,7 +325,8 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_plan(int dtype, int64_t M, int64_t N, in
  * where the shape allows them.  split: -1
  * automatic, 0 every tile whole (no stream-K split), 1 split wherever the
  * schedule can (also where the automatic rule keeps whole tiles: a nearly
- * full last wave, a modest cut in k-blocks per CTA, memory-bound shapes
+ * full last wave -- for quads one more than half full, or fewer than two
+ * full waves --, a modest cut in k-blocks per CTA, memory-bound shapes
  * whose tiles already fill half the grid).  Returns INVALID_VALUE for values
  * outside these sets.
  */
@@ -386,8 +387,8 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_test_inject_stall(int64_t k_block, int t
  * Test hook that shows the pipelining ("Pipeline GPU Kernel", Steps 3-4:
  * the loads of the next K-tiles are issued while the tensor cores work on
  * this one).  For the next GEMM launch only, and when that launch runs the
- * FP16 CTA-pair kernel with 256-wide tiles and a 6- or 1-stage ring, or
- * with 512-wide tiles (the kernels compiled with the trace; any other
+ * FP16 CTA-pair kernel with 256-wide tiles and a 6- or 1-stage ring, with
+ * 512-wide tiles, or on quads (the kernels compiled with the trace; any other
  * launch consumes the hook and records nothing),
  * CTA 0 (the leader CTA of pair 0) writes %globaltimer nanoseconds into `buffer`, a
  * device array of 3 * `entries` uint64: element j (j < entries) when its
