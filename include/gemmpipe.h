@@ -335,10 +335,9 @@ GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_override(int producer, int bn, 
 
 /*
  * Test hook: k values per pipeline stage for the following calls of this
- * process (0 automatic: 128 on CTA pairs and on fp16 single-CTA plans with
- * N <= 128, unless a ring depth is forced, 64 elsewhere; 64; or 128: 64 KiB
- * stages, three deep -- on CTA pairs, and on single CTAs with 128 x 128
- * fp16 tiles).  Plans without a 128-k variant
+ * process (0 automatic: 128 on fp16 single-CTA plans with N <= 128 unless
+ * a ring depth is forced, 64 elsewhere; 64; or 128: 64 KiB stages, three
+ * deep -- on CTA pairs, and on single CTAs with 128 x 128 fp16 tiles).  Plans without a 128-k variant
  * keep 64.  Returns INVALID_VALUE for other values.
  */
 GEMMPIPE_API gemmpipe_status_t gemmpipe_set_plan_bk(int bk);

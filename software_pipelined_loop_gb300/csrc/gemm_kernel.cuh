@@ -795,7 +795,7 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
 // quad to the other pair too, whose A copies also land in these stages.
 template <class Cfg>
 __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
-                                Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, uint32_t crank)
+                                Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, uint32_t crank, int lane)
 {
     constexpr uint32_t idesc = umma_idesc_f16_f32(2 * Cfg::BM, Cfg::MMA_N, true);
     const uint16_t BOTH = static_cast<uint16_t>(3u << crank);              // this pair's two CTAs
@@ -815,43 +815,48 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
     while (ok && it.next(p, wk)) {
         for (int64_t kc = wk.kb0; kc < wk.kb1 && ok; kc += p.kb_per_chunk) {
             const int64_t kend = kc + p.kb_per_chunk < wk.kb1 ? kc + p.kb_per_chunk : wk.kb1;
-            if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
+            if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u))) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
             const uint32_t d = tmem_base + acc * Cfg::BN;
             for (int64_t kb = kc; kb < kend; ++kb) {
-                if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
+                if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->full[stage]), phase))) {
                     ok = false;
                     break;
                 }
                 if constexpr (Cfg::TRACE) {
-                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
+                    if (lane == 0 && p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
                         p.trace[p.trace_n + nkb] = globaltimer_ns();
                         p.trace[2 * p.trace_n + nkb] = sm_clock64();
                     }
                     ++nkb;
+                    __syncwarp();  // converged again for elect.sync
                 }
                 tc_fence_after_sync();
                 const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
+                if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 16; ++kk)
+                    for (int kk = 0; kk < Cfg::BK / 16; ++kk)
 #pragma unroll
-                    for (int u = 0; u < Cfg::N_MMAS; ++u)
-                        umma_f16_pair(d + u * Cfg::MMA_N,
-                                      dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
-                                      dB0 + so + ((u * B_MMA_BYTES + kk * 2048) >> 4), idesc,
-                                      (kb > kc || kk > 0) ? 1u : 0u);
+                        for (int u = 0; u < Cfg::N_MMAS; ++u)
+                            umma_f16_pair(d + u * Cfg::MMA_N,
+                                          dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
+                                          dB0 + so + ((u * B_MMA_BYTES + kk * 2048) >> 4), idesc,
+                                          (kb > kc || kk > 0) ? 1u : 0u);
+                    umma_commit_pair(smem_u32(&ctl->empty[stage]), STAGE_MASK);
+                }
+                __syncwarp();
                 issued = true;
-                umma_commit_pair(smem_u32(&ctl->empty[stage]), STAGE_MASK);
                 if (++stage == Cfg::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit_pair(smem_u32(&ctl->tfull[acc]), BOTH);
+            if (elect_one_sync()) umma_commit_pair(smem_u32(&ctl->tfull[acc]), BOTH);
+            __syncwarp();
             if constexpr (Cfg::ACC_BUFS == 2) {
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
@@ -865,12 +870,14 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
         // epilogue arrivals on these barriers -- have landed before the
         // pair's final (relaxed) cluster barrier.  The parities are the
         // ones the next use of each buffer would wait for.
-        ok = w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u);
+        ok = __all_sync(0xffffffffu, w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u));
         if constexpr (Cfg::ACC_BUFS == 2)
-            ok = ok && w.wait(smem_u32(&ctl->tempty[acc ^ 1u]), acc == 0 ? acc_phase ^ 1u : acc_phase);
+            ok = ok && __all_sync(0xffffffffu, w.wait(smem_u32(&ctl->tempty[acc ^ 1u]),
+                                                      acc == 0 ? acc_phase ^ 1u : acc_phase));
     }
     if (!ok && issued) {
-        umma_commit_pair(smem_u32(&ctl->drain), static_cast<uint16_t>(1u << crank));
+        if (elect_one_sync()) umma_commit_pair(smem_u32(&ctl->drain), static_cast<uint16_t>(1u << crank));
+        __syncwarp();
         w.wait_drain(smem_u32(&ctl->drain), 0, kDrainNs);
     }
 }
@@ -879,7 +886,7 @@ __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tm
 
 template <class Cfg>
 __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
-                           Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
+                           Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w, int lane)
 {
     constexpr uint32_t idesc = umma_idesc_f16_f32(Cfg::BM, Cfg::BN, true);
     // Stage s, k-step kk of the ring differ from stage 0, k-step 0 only in
@@ -897,49 +904,55 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
     while (ok && it.next(p, wk)) {
         for (int64_t kc = wk.kb0; kc < wk.kb1 && ok; kc += p.kb_per_chunk) {
             const int64_t kend = kc + p.kb_per_chunk < wk.kb1 ? kc + p.kb_per_chunk : wk.kb1;
-            if (!w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u)) {
+            if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u))) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
             const uint32_t d = tmem_base + acc * Cfg::BN;
             for (int64_t kb = kc; kb < kend; ++kb) {
-                if (!w.wait(smem_u32(&ctl->full[stage]), phase)) {
+                if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->full[stage]), phase))) {
                     ok = false;
                     break;
                 }
                 if constexpr (Cfg::TRACE) {
-                    if (p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
+                    if (lane == 0 && p.trace && blockIdx.x == 0 && nkb < p.trace_n) {
                         p.trace[p.trace_n + nkb] = globaltimer_ns();
                         p.trace[2 * p.trace_n + nkb] = sm_clock64();
                     }
                     ++nkb;
+                    __syncwarp();  // converged again for elect.sync
                 }
                 tc_fence_after_sync();
                 const uint64_t so = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
-                umma_f16(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
-                // k-step kk: A sub-tile kk / 4 (64 k each), 32 bytes per
-                // 16 k within it; B 16 rows of its atoms per 16 k.
+                if (elect_one_sync()) {
+                    umma_f16(d, dA0 + so, dB0 + so, idesc, kb > kc ? 1u : 0u);
+                    // k-step kk: A sub-tile kk / 4 (64 k each), 32 bytes per
+                    // 16 k within it; B 16 rows of its atoms per 16 k.
 #pragma unroll
-                for (int kk = 1; kk < Cfg::BK / 16; ++kk)
-                    umma_f16(d, dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
-                             dB0 + so + (kk * 2048 >> 4), idesc, 1u);
+                    for (int kk = 1; kk < Cfg::BK / 16; ++kk)
+                        umma_f16(d, dA0 + so + (((kk / 4) * Cfg::A_SUB_BYTES + (kk % 4) * 32) >> 4),
+                                 dB0 + so + (kk * 2048 >> 4), idesc, 1u);
+                    umma_commit(smem_u32(&ctl->empty[stage]));
+                }
+                __syncwarp();
                 issued = true;
-                umma_commit(smem_u32(&ctl->empty[stage]));
                 if (++stage == Cfg::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit(smem_u32(&ctl->tfull[acc]));
+            if (elect_one_sync()) umma_commit(smem_u32(&ctl->tfull[acc]));
+            __syncwarp();
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
     if (!ok && issued) {
-        // Every MMA this thread issued must finish before TMEM is freed.
-        umma_commit(smem_u32(&ctl->drain));
+        // Every MMA this warp issued must finish before TMEM is freed.
+        if (elect_one_sync()) umma_commit(smem_u32(&ctl->drain));
+        __syncwarp();
         w.wait_drain(smem_u32(&ctl->drain), 0, kDrainNs);
     }
 }
@@ -1346,9 +1359,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             } else if (warp == Cfg::MMA_WARP) {
                 if constexpr (Cfg::PAIR) {
-                    if (lane == 0 && pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank);
+                    if (pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank, lane);
                 } else {
-                    if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+                    mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w, lane);
                 }
                 __syncwarp();
             }
@@ -1368,9 +1381,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if constexpr (Cfg::CONVERT) converter<Cfg>(p, sbase, ctl, w);
     } else if (warp == Cfg::MMA_WARP) {
         if constexpr (Cfg::PAIR) {
-            if (lane == 0 && pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank);
+            if (pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank, lane);
         } else {
-            if (lane == 0) mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w);
+            mma_issuer<Cfg>(p, sbase, tmem_base, ctl, w, lane);
         }
         __syncwarp();
     } else {

@@ -281,11 +281,12 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     const bool want_quad = ov.pair == 2 || (ov.pair == -1 && !c_aligned && !convert);
     if (producer == 0 && bn >= 256 && M > kBM && N > 128 && ov.pair != 0) {
         if (want_quad && bn == 256) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 2);
-        // CTA pairs take 128 k per stage unless a ring depth or 64 k is asked
-        // for (A/B in one process, kernel time: INT8 4096^3 86.4 vs 87.9 us,
-        // FP16 4096^3 87.1 vs 87.7, INT8 1024 x 4096^2 31.5 vs 32.8, FP16
-        // 3072^3 42.5 vs 43.3; ragged FP16 and INT8 8192^3 within +1.2%).
-        const bool bk128 = ov.bk == 128 || (ov.bk == 0 && ov.stages == 0);
+        // CTA pairs take six stages of 64 k; 128 k per stage (three stages)
+        // only when asked for.  With the MMA issue on the whole warp, 64-k
+        // stages measured faster (A/B in one process, kernel time: FP16
+        // 4096^3 84.9 vs 87.9 us, INT8 4096^3 83.1 vs 84.8, FP16 8192^3 596
+        // vs 604, 2048 x 4096^2 50.0 vs 52.5, 6144^3 258.2 vs 263.3).
+        const bool bk128 = ov.bk == 128;
         if (!v && bk128) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1, 128);
         if (!v) v = find_variant(int_out, convert ? 1 : 0, 0, bn, ov.stages, 1);
         if (!v && bn == 512) v = find_variant(int_out, convert ? 1 : 0, 0, 256, ov.stages, 1);

@@ -337,6 +337,20 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// True in exactly one lane of the calling (converged, full) warp.  Code
+// that the whole warp runs keeps its operands warp-uniform, and the one
+// elected lane issues the single-thread instructions (tcgen05.mma, commit).
+__device__ __forceinline__ bool elect_one_sync()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
