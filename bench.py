@@ -640,14 +640,14 @@ SQUARE = (4096, 4096, 4096)
 RAGGED = (4093, 3001, 4107)
 SKINNY = (16384, 128, 16384)
 ABLATION = [
-    # (label, dtype, shape, producer, bn, stages, cta_pair, split)
+    # (label, dtype, shape, producer, bn, stages, cta_pair, split[, k per stage])
     ("pair S=1 (load, wait, compute)", "f16", SQUARE, 0, 256, 1, 1, -1),
     ("pair S=2 (double buffer)", "f16", SQUARE, 0, 256, 2, 1, -1),
     ("pair S=3", "f16", SQUARE, 0, 256, 3, 1, -1),
     ("pair S=4", "f16", SQUARE, 0, 256, 4, 1, -1),
     ("pair S=5", "f16", SQUARE, 0, 256, 5, 1, -1),
-    ("pair S=6", "f16", SQUARE, 0, 256, 6, 1, -1),
-    ("pair, 128 k per stage, S=3 (default)", "f16", SQUARE, 0, 256, 0, 1, -1),
+    ("pair S=6 (default)", "f16", SQUARE, 0, 256, 6, 1, -1),
+    ("pair, 128 k per stage, S=3", "f16", SQUARE, 0, 256, 0, 1, -1, 128),
     ("pair S=6, every tile whole (no stream-K)", "f16", SQUARE, 0, 256, 6, 1, 0),
     ("single CTA 128x256 S=4", "f16", SQUARE, 0, 256, 4, 0, -1),
     ("single CTA 128x128 S=6", "f16", SQUARE, 0, 128, 6, 0, -1),
@@ -685,7 +685,8 @@ def run_ablation(args) -> int:
 
     ops = {}
     rows = []
-    for label, dt, shape, producer, bn, stages, pair, split in ABLATION:
+    for label, dt, shape, producer, bn, stages, pair, split, *rest in ABLATION:
+        bk = rest[0] if rest else 0  # k per stage (0: the planner's choice)
         M, N, K = shape
         if (dt, shape) not in ops:
             A, B = inputs.make_operands(dt, M, N, K, inputs.SEED_BASE + 5)
@@ -696,6 +697,7 @@ def run_ablation(args) -> int:
         fn = gemmpipe.gemm_s8s8s32 if dt == "s8" else gemmpipe.gemm_f16f32
         stream = torch.cuda.current_stream(dev)
         gemmpipe.gemmpipe_set_plan_override(producer, bn, stages, pair, split)
+        gemmpipe.gemmpipe_set_plan_bk(bk)
         try:
             plan = gemmpipe.gemmpipe_plan(0 if dt == "s8" else 1, M, N, K, Ad, Bd, C)
             call = lambda: fn(M, N, K, Ad, Bd, C, stream)
@@ -709,13 +711,14 @@ def run_ablation(args) -> int:
             gemmpipe.gemmpipe_timing_enable(False)
         finally:
             gemmpipe.gemmpipe_set_plan_override(-1, 0, 0, -1, -1)
+            gemmpipe.gemmpipe_set_plan_bk(0)
         st = gemmpipe.gemmpipe_get_device_status(stream)
         ms = statistics.mean(times)
         kms = gms / max(1, gn)
         rows.append({"config": label, "shape": list(shape), "ms_per_step": ms,
                      "per_step": 2.0 * M * N * K / ms / 1e9, "kernel_ms": kms,
                      "per_kernel": 2.0 * M * N * K / kms / 1e9, "status": st,
-                     "plan": {k: plan[k] for k in ("producer", "BM", "BN", "stages", "cta_pair", "units",
+                     "plan": {k: plan[k] for k in ("producer", "BM", "BN", "BK", "stages", "cta_pair", "units",
                                                    "split_tiles", "operand_copy")}})
     base = rows[0]["ms_per_step"]
     for r in rows:
