@@ -510,6 +510,7 @@ template <class Cfg>
 __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const CUtensorMap *tB,
                              uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w)
 {
+    // The whole producer warp runs the loop; one elected lane issues.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arm
@@ -521,11 +522,12 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
         const int32_t m0 = static_cast<int32_t>(wk.m0);
         const int32_t n0 = static_cast<int32_t>(wk.n0);
         for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
-            if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
+            if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u))) {
                 ok = false;
                 break;
             }
             if (!(blockIdx.x == 0 && kb_count == p.stall_kb)) {
+              if (elect_one_sync()) {
                 const uint32_t fb = smem_u32(&ctl->full[stage]);
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
                 const int32_t k0 = static_cast<int32_t>(kb * Cfg::BK);
@@ -538,6 +540,8 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
                 if constexpr (Cfg::TRACE) {
                     if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
                 }
+              }
+                __syncwarp();
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -548,7 +552,7 @@ __device__ void producer_tma(const GemmParams &p, const CUtensorMap *tA, const C
         }
     }
     if (!ok) {
-        // Let every copy this thread started land before the CTA exits.
+        // Let every copy this warp started land before the CTA exits.
         for (int s = 0; s < Cfg::STAGES; ++s)
             if (armed & (1u << s))
                 w.wait_drain(smem_u32(&ctl->full[s]), (armed_par >> s) & 1u, kDrainNs);
@@ -699,6 +703,8 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                                   uint32_t sbase, Ctl<Cfg::STAGES, Cfg::I8_STAGES> *ctl, const Waiter &w,
                                   uint32_t crank)
 {
+    // The whole producer warp runs the loop (its state and the copies'
+    // coordinates stay warp-uniform); one elected lane issues the copies.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_par = 0;
@@ -722,11 +728,12 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
         // that MMA's MMA_N columns (a quad's second pair: the next BN).
         const int32_t n0 = static_cast<int32_t>(wk.n0 + pair_i * Cfg::BN + rank * (Cfg::MMA_N / 2));
         for (int64_t kb = wk.kb0; kb < wk.kb1; ++kb, ++kb_count) {
-            if (!w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u)) {
+            if (!__all_sync(0xffffffffu, w.wait(smem_u32(&ctl->empty[stage]), phase ^ 1u))) {
                 ok = false;
                 break;
             }
             if (!(stall_cta && kb_count == p.stall_kb)) {
+              if (elect_one_sync()) {
                 const uint32_t fb_local = full0 + 8u * static_cast<uint32_t>(stage);
                 const uint32_t fb = full0_leader + 8u * static_cast<uint32_t>(stage);  // the leader's full[s]
                 const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
@@ -756,6 +763,8 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
                 if constexpr (Cfg::TRACE) {
                     if (p.trace && blockIdx.x == 0 && kb_count < p.trace_n) p.trace[kb_count] = globaltimer_ns();
                 }
+              }
+                __syncwarp();
                 armed |= 1u << stage;
                 armed_par = phase ? (armed_par | (1u << stage)) : (armed_par & ~(1u << stage));
             }
@@ -771,7 +780,7 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
         // each stage's last phase so none is still in flight at exit.
         for (int s = 0; s < Cfg::STAGES && ok; ++s) {
             const uint32_t ph = s < stage ? phase ^ 1u : phase;  // phase of the stage's next use
-            ok = w.wait(smem_u32(&ctl->empty[s]), ph ^ 1u);
+            ok = __all_sync(0xffffffffu, w.wait(smem_u32(&ctl->empty[s]), ph ^ 1u));
         }
     }
     if (!ok) {
@@ -1351,12 +1360,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (warp < 4) {
             setmaxnreg_dec<Cfg::CTRL_REGS>();
             if (warp == 0) {
-                if (lane == 0) {
-                    if constexpr (Cfg::PAIR)
-                        producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
-                    else
-                        producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
-                }
+                if constexpr (Cfg::PAIR)
+                    producer_tma_pair<Cfg>(p, &tmA, &tmB, sbase, ctl, w, rank);
+                else
+                    producer_tma<Cfg>(p, &tmA, &tmB, sbase, ctl, w);
+                __syncwarp();
             } else if (warp == Cfg::MMA_WARP) {
                 if constexpr (Cfg::PAIR) {
                     if (pair_leader) mma_issuer_pair<Cfg>(p, sbase, tmem_base, ctl, w, rank, lane);
