@@ -73,10 +73,10 @@ KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "launch_impl.cu
                   "gemmpipe_api.cpp"]
 TRAFFIC = {
     # (dtype, M, N, K, cta pair, BN, BK): (bytes per launch, sources hash)
-    ("s8", 4096, 4096, 4096, 1, 256, 64): (138_538_496, "79fbe751f8c2dfce"),
-    ("f16", 4096, 4096, 4096, 1, 256, 64): (138_780_672, "79fbe751f8c2dfce"),
-    ("f16", 16384, 128, 16384, 0, 128, 128): (544_314_880, "79fbe751f8c2dfce"),
-    ("f16", 4093, 3001, 4107, 2, 512, 64): (69_998_592, "79fbe751f8c2dfce"),
+    ("s8", 4096, 4096, 4096, 1, 256, 64): (137_490_944, "dfd2a3c1cd53f52e"),
+    ("f16", 4096, 4096, 4096, 1, 256, 64): (138_108_672, "dfd2a3c1cd53f52e"),
+    ("f16", 16384, 128, 16384, 0, 128, 128): (544_086_016, "dfd2a3c1cd53f52e"),
+    ("f16", 4093, 3001, 4107, 2, 512, 64): (67_184_128, "dfd2a3c1cd53f52e"),
 }
 
 
