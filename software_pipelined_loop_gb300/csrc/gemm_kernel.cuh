@@ -7,13 +7,13 @@
 // Here the same schedule is spread over warps with separate jobs and the
 // double buffer becomes an S-stage ring guarded by mbarriers:
 //
-//   producer  (1 thread issuing TMA tile loads, or 8 warps doing
+//   producer  (1 warp issuing TMA tile loads, or 8 warps doing
 //             bounds-checked loads into registers and shared-memory stores --
 //             the page's LDG-register variant, used when TMA cannot describe
 //             the input) waits empty[s], fills stage s with the A tile
 //             (BM x BK) and the B tile (BK x BN) of k-block kb, and signals
 //             full[s];
-//   issuer    (one thread) waits full[s], issues BK/16 tcgen05.mma (K = 16;
+//   issuer    (1 warp) waits full[s], issues BK/16 tcgen05.mma (K = 16;
 //             M = 256 over a CTA pair with cta_group::2, else 128) into a
 //             TMEM accumulator, then tcgen05.commit -> empty[s] returns the
 //             stage to the producer as soon as the tensor cores have read it;
@@ -21,6 +21,11 @@
 //             with tcgen05.ld, frees it, and stores C through a per-warp
 //             staging tile (one TMA store per 32 x 32 block, or
 //             row-contiguous masked stores).
+//
+// The TMA producer and the issuer run their loops on the whole warp, one
+// elected lane issuing the copies, MMAs and commits: the loop state and the
+// descriptors stay warp-uniform, and the coupled ring keeps the tensor pipe
+// fed (with a single thread per role, the same pipeline ran ~25% slower).
 //
 // The page's prologue is the producer running up to S stages ahead; its
 // "compute the last tile" epilogue is the issuer's final commit on tfull.
@@ -799,8 +804,8 @@ __device__ void producer_tma_pair(const GemmParams &p, const CUtensorMap *tA, co
     }
 }
 
-// Leader CTA only (cluster rank `crank`, even): one thread issues the
-// pair's MMAs.  A stage is released to both CTAs of the pair -- and in a
+// Leader CTA only (cluster rank `crank`, even): its MMA warp issues the
+// pair's MMAs (one elected lane).  A stage is released to both CTAs of the pair -- and in a
 // quad to the other pair too, whose A copies also land in these stages.
 template <class Cfg>
 __device__ void mma_issuer_pair(const GemmParams &p, uint32_t sbase, uint32_t tmem_base,
