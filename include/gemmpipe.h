@@ -37,7 +37,8 @@
  * (device, stream) holds stream-K partial sums: when the output tiles leave
  * the persistent grid's last wave at most 4/5 full (or, with fewer tiles
  * than the grid holds, when spreading them cuts each CTA's k-blocks to a
- * third or less), the k-blocks of the last waves' tiles are split into equal
+ * third or less -- on single CTAs of a compute-bound GEMM, by 1536 k values
+ * or more), the k-blocks of the last waves' tiles are split into equal
  * ranges over all CTAs and a split tile's parts
  * are added by the CTA holding its last k-block (128 x BN x 4 bytes per CTA
  * plus 64 KiB of flags; if it cannot be allocated, every tile runs whole

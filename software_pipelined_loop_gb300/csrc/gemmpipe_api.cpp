@@ -167,6 +167,9 @@ constexpr int64_t kSplitFlagBytes = kMaxSplitCtas * kSplitFlagsPerCta * 4;
 // grid: below this the ring's fill and the fix-up cost more than the idle
 // SMs they replace.
 constexpr int64_t kMinSplitKb = 8;
+// Fewest k values a split must take off each single-CTA unit to pay for
+// its fix-up when there are fewer tiles than units.
+constexpr int64_t kMinSavedK = 1536;
 
 // Dense fp16 tensor flops per byte of HBM traffic at which GB300 turns from
 // memory- to compute-bound (about 2.2 PFLOP/s over 7.9 TB/s; a copy and a
@@ -321,9 +324,16 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     // all units as equal ranges of k-blocks (stream-K), so every unit does
     // the same work.  With fewer tiles than slots, all tiles are split over
     // as many units as keep at least kMinSplitKb k-blocks each, when that
-    // cuts a unit's k-blocks to a third or less.  Measured on GB300: a
-    // split costs its fix-up and, with every SM streaming operands at once,
-    // a slower k-loop, so it pays only when the work per unit drops a lot.
+    // cuts a unit's k-blocks to a third or less -- or, on single CTAs of a
+    // compute-bound GEMM, by kMinSavedK k values or more.  Measured on
+    // GB300: a split costs its fix-up and, with every SM streaming operands
+    // at once, a slower k-loop (about 7 us on single CTAs), so it pays only
+    // when the work per unit drops a lot.  Single CTAs, M = N = 1024 (64
+    // tiles on 152 units), call time whole vs split: K = 2048 16.7 vs 18.7
+    // us (1152 k fewer per unit), 3072 20.8 vs 19.3 (1728), 4096 23.4 vs
+    // 21.0, 8192 38.9 vs 27.2; INT8 K = 2048 20.8 vs 21.4, 4096 29.5 vs
+    // 27.1.  CTA pairs with 32 to 64 tiles on 76 pairs (N = K = 4096) stay
+    // faster whole.
     // Quads (the plan for C rows off 16-byte boundaries, whose row-piece
     // stores make every item's epilogue long) split only a last wave at
     // most half full after two or more full waves (measured: 96 tiles on 36
@@ -345,7 +355,10 @@ gemmpipe_status_t make_plan(bool int_out, int64_t M, int64_t N, int64_t K, const
     if (split && T < slots) {
         const int64_t want = (T * pl->num_kb + kMinSplitKb - 1) / kMinSplitKb;
         const int64_t u = want < slots ? want : slots;
-        if (u > T && (ov.split == 1 || (u >= 3 * T && !(memory_bound && 2 * T >= slots)))) {
+        // k values a unit computes fewer than with whole tiles.
+        const int64_t saved_k = u > T ? (pl->num_kb - (T * pl->num_kb + u - 1) / u) * bk : 0;
+        const bool pays = u >= 3 * T || (v->info.pair == 0 && !memory_bound && saved_k >= kMinSavedK);
+        if (u > T && (ov.split == 1 || (pays && !(memory_bound && 2 * T >= slots)))) {
             pl->units = u;
             pl->dp_tiles = 0;
             pl->sk_tiles = T;

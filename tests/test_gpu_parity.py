@@ -832,6 +832,26 @@ def test_small_problems_take_single_cta_tiles(dev, dtype, M, N, K, small):
         assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
 
 
+@pytest.mark.parametrize("dtype", ["f16", "s8"])
+@pytest.mark.parametrize("M,N,K,split", [(1024, 1024, 2048, False), (1024, 1024, 3072, True),
+                                         (1000, 1000, 4100, True), (1024, 896, 4096, True)])
+def test_single_cta_tiles_split_long_k(dev, dtype, M, N, K, split):
+    # Fewer single-CTA tiles than SMs: the planner spreads the k-blocks over
+    # all SMs when that takes at least 1536 k values off each unit (whole
+    # tiles otherwise).  Results match the oracle either way.
+    plan = gemmpipe.gemmpipe_plan(0 if dtype == "s8" else 1, M, N, K)
+    assert plan["cta_pair"] == 0 and plan["BN"] == 128
+    if split:
+        assert plan["split_tiles"] == plan["tiles"] and plan["units"] > plan["tiles"]
+    else:
+        assert plan["split_tiles"] == 0 and plan["units"] == plan["tiles"]
+    A, B = inputs.make_operands(dtype, M, N, K, seed=970 + M + K)
+    if dtype == "s8":
+        np.testing.assert_array_equal(run_s8(A, B, dev), oracle.gemm_s8s8s32(A, B))
+    else:
+        assert_f16_close(run_f16(A, B, dev), oracle.gemm_f16f32(A, B))
+
+
 # ------------------------------------------- quads: two CTA pairs sharing A
 
 @pytest.mark.parametrize("split", [-1, 0, 1], ids=["auto", "whole", "split"])

@@ -18,8 +18,9 @@ k-block counts, that
 
 The grid choice mirrors the library's planner: tiles < slots splits all
 tiles over u = min(slots, ceil(tiles * k_blocks / 8)) units when u is at
-least three times the tile count (unless the GEMM is memory-bound and its
-tiles already fill half the slots); more tiles than slots with a partial
+least three times the tile count, or (single CTAs, compute-bound GEMMs)
+when that takes 1536 k values or more off each unit (unless the GEMM is
+memory-bound and its tiles already fill half the slots); more tiles than slots with a partial
 last wave at most 4/5 full split the last two waves' tiles (slots + tiles %
 slots) over all slots -- for quads (the plan for C rows off 16-byte
 boundaries) only a last wave at most half full after two full waves.  `force` is the plan override that splits wherever
@@ -32,16 +33,19 @@ import itertools
 import pytest
 
 MIN_SPLIT_KB = 8
+MIN_SAVED_K = 1536
 
 
 def plan(tiles: int, slots: int, num_kb: int, memory_bound: bool = False, force: bool = False,
-         quad: bool = False):
+         quad: bool = False, single: bool = False, bk: int = 64):
     units, dp_tiles, sk_tiles = min(tiles, slots), tiles, 0
     tail = tiles % slots
     tail_rule = (2 * tail <= slots and tiles >= 2 * slots) if quad else 5 * tail <= 4 * slots
     if tiles < slots:
         u = min(slots, -(-tiles * num_kb // MIN_SPLIT_KB))
-        if u > tiles and (force or (u >= 3 * tiles and not (memory_bound and 2 * tiles >= slots))):
+        saved_k = (num_kb - -(-tiles * num_kb // u)) * bk if u > tiles else 0
+        pays = u >= 3 * tiles or (single and not memory_bound and saved_k >= MIN_SAVED_K)
+        if u > tiles and (force or (pays and not (memory_bound and 2 * tiles >= slots))):
             units, dp_tiles, sk_tiles = u, 0, tiles
     elif tiles > slots and tail and num_kb > 1 and (force or tail_rule):
         sk_tiles = slots + tiles % slots
@@ -196,3 +200,26 @@ def test_quad_split_rule_matches_the_measured_cases():
     assert plan(96, 36, 65)[2] == 36 + 96 % 36
     # Forced splits ignore both rules; the schedule invariants hold either way.
     assert plan(96, 36, 65, quad=True, force=True)[2] == 36 + 96 % 36
+
+
+def test_single_cta_split_rule_matches_the_measured_cases():
+    # Single CTAs, M = N = 1024 (64 tiles on 152 SMs), 64-k blocks: the
+    # split measured faster from K = 3072 on, slower at K = 2048.
+    assert plan(64, 152, 32, single=True)[2] == 0          # K = 2048: 1152 k fewer per unit
+    assert plan(64, 152, 48, single=True)[2] == 64         # K = 3072: 1728
+    assert plan(64, 152, 64, single=True)[2] == 64         # K = 4096
+    assert plan(64, 152, 128, single=True)[2] == 64        # K = 8192
+    assert plan(64, 152, 16, single=True)[2] == 0          # 1024^3: u = 128 units of 8 k-blocks
+    # Memory-bound shapes and CTA pairs keep the older rule.
+    assert plan(64, 152, 64, single=True, memory_bound=True)[2] == 0
+    assert plan(32, 76, 64)[2] == 0 and plan(48, 76, 64)[2] == 0 and plan(64, 76, 64)[2] == 0
+    # The schedule invariants hold for the new splits too.
+    for num_kb in (48, 64, 128):
+        units, dp, sk = plan(64, 152, num_kb, single=True)
+        seen = {}
+        for u in range(units):
+            for t, kb0, kb1, _ in items(u, units, dp, sk, num_kb):
+                for kb in range(kb0, kb1):
+                    assert (t, kb) not in seen
+                    seen[(t, kb)] = u
+        assert len(seen) == 64 * num_kb
