@@ -977,12 +977,14 @@ __device__ void mma_issuer(const GemmParams &p, uint32_t sbase, uint32_t tmem_ba
 // columns col0 .. col0 + 31.  The block goes through the warp's staging tile
 // (16-byte chunks XOR-swizzled by row, conflict-free both ways) so that each
 // global store instruction writes whole 128-byte row pieces.
-template <bool ADD = false>
+// TMA = false keeps the block on the load/store path even where C takes TMA
+// stores (C that a later chunk reads back and adds to).
+template <bool ADD = false, bool TMA = true>
 __device__ __forceinline__ void store_block(const GemmParams &p, const CUtensorMap *tC, uint32_t stg,
                                             const uint32_t *r, int64_t row0, int64_t col0, int lane)
 {
     if (row0 >= p.M || col0 >= p.N) return;  // warp-uniform
-    if (!ADD && p.tma_store) {
+    if (!ADD && TMA && p.tma_store) {
         // The staging tile is in the 128-byte swizzle the C tensor map
         // declares; one TMA store writes the block (clipped at M and N).
         if (lane == 0) bulk_wait_read<0>();  // the previous block's store has read the tile
@@ -999,6 +1001,7 @@ __device__ __forceinline__ void store_block(const GemmParams &p, const CUtensorM
         }
         return;
     }
+    __syncwarp();  // every lane has read the previous block out of the staging tile
 #pragma unroll
     for (int c = 0; c < 8; ++c)
         st_shared_v4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
@@ -1199,8 +1202,10 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * NCOLS;
             if constexpr (Cfg::SUM_IN_C) {
                 // Whole tiles only.  Chunk partials are exact integers; the
-                // first chunk stores them, later chunks add into C (each
-                // element is read and written by the same thread, in order).
+                // first chunk stores them, later chunks add into C.  Every
+                // chunk goes through the load/store path, so a later chunk's
+                // reads follow the earlier chunk's writes in this warp's own
+                // program order (a TMA store would complete asynchronously).
 #pragma unroll
                 for (int jb = 0; jb < NB; ++jb) {
                     uint32_t r[32];
@@ -1209,9 +1214,9 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
                     if (kc == wk.kb0)
-                        store_block<false>(p, tC, stg, r, row0, colb + jb * 32, lane);
+                        store_block<false, false>(p, tC, stg, r, row0, colb + jb * 32, lane);
                     else
-                        store_block<true>(p, tC, stg, r, row0, colb + jb * 32, lane);
+                        store_block<true, false>(p, tC, stg, r, row0, colb + jb * 32, lane);
                 }
             } else if constexpr (ISUM) {
                 // Chunk partials are integers below 2^24 in magnitude: exact
