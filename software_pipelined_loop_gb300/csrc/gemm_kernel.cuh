@@ -1202,10 +1202,12 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * Cfg::BN + h * NCOLS;
             if constexpr (Cfg::SUM_IN_C) {
                 // Whole tiles only.  Chunk partials are exact integers; the
-                // first chunk stores them, later chunks add into C.  Every
-                // chunk goes through the load/store path, so a later chunk's
-                // reads follow the earlier chunk's writes in this warp's own
-                // program order (a TMA store would complete asynchronously).
+                // first chunk stores them, later chunks add into C.  When a
+                // later chunk will read C back, every chunk goes through the
+                // load/store path, so its reads follow the earlier chunk's
+                // writes in this warp's own program order (a TMA store
+                // completes asynchronously); a single chunk may use TMA.
+                const bool one_chunk = wk.kb1 - wk.kb0 <= p.kb_per_chunk;
 #pragma unroll
                 for (int jb = 0; jb < NB; ++jb) {
                     uint32_t r[32];
@@ -1213,7 +1215,9 @@ __device__ void epilogue(const GemmParams &p, const CUtensorMap *tC, uint32_t sb
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[i])));
-                    if (kc == wk.kb0)
+                    if (one_chunk)
+                        store_block<false, true>(p, tC, stg, r, row0, colb + jb * 32, lane);
+                    else if (kc == wk.kb0)
                         store_block<false, false>(p, tC, stg, r, row0, colb + jb * 32, lane);
                     else
                         store_block<true, false>(p, tC, stg, r, row0, colb + jb * 32, lane);
