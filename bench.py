@@ -80,14 +80,16 @@ TRAFFIC = {
 }
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources' code: comments and blank space are left
-    out, so an edit to a comment keeps the captured figures valid."""
+def kernel_source_hash(csrc: str | None = None) -> str:
+    """Hash of the kernel sources' code (in `csrc`, default the package's):
+    comments and blank space are left out, so an edit to a comment keeps the
+    captured figures valid."""
     import hashlib
     import re
+    csrc = csrc or os.path.join(ROOT, "software_pipelined_loop_gb300", "csrc")
     h = hashlib.sha1()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "software_pipelined_loop_gb300", "csrc", f), encoding="utf-8") as fh:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
         text = re.sub(r"//[^\n]*", " ", text)               # line comments
